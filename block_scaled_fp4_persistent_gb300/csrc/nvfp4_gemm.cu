@@ -1,0 +1,593 @@
+// nvfp4_gemm.cu -- host side of the grouped NVFP4 GEMM library and its C ABI.
+//
+// One call runs through these steps:
+//  1. Check every argument on the host. Nothing is queued when a check fails.
+//  2. Clear C with cudaMemsetAsync for K == 0 groups (the empty sum).
+//  3. For row-major scales, run the prepack kernel into a per-stream workspace.
+//  4. Find the device table for this problem set: tensor maps, per-group
+//     pointers and the per-CTA tile lists. It is cached under an FNV-1a hash of
+//     the problem set. On a miss it is built on the host and uploaded with one
+//     cudaMemcpyAsync.
+//  5. Launch the persistent kernel: one launch for all groups.
+//
+// The pages cache their launch state the same way, because encoding tensor maps
+// is a costly driver call (page 1, `group_gemm`, the FNV-1a keyed caches; page 2,
+// `LaunchCache`).
+#include <cuda_runtime.h>
+#include <cudaTypedefs.h>
+
+#include <algorithm>
+#include <atomic>
+#include <cstdio>
+#include <cstring>
+#include <list>
+#include <map>
+#include <mutex>
+#include <unordered_map>
+#include <vector>
+
+#include "nvfp4_grouped_gemm.h"
+#include "gemm_kernel.cuh"
+#include "prepack.cuh"
+#include "table.h"
+
+using namespace nvfp4;
+
+namespace {
+
+// ------------------------------------------------------------------ state --
+
+std::atomic<int> g_last_cuda_error{0};
+
+struct Options {
+    std::atomic<int64_t> block_n{0};
+    std::atomic<int64_t> stages{0};
+    std::atomic<int64_t> max_ctas{0};
+    std::atomic<int64_t> timeout_us{2000000};
+    std::atomic<int64_t> fault_skip_load{-1};
+} g_opt;
+
+constexpr int kMaxDevices = 64;
+constexpr int kMaxDim = 1 << 24;
+constexpr size_t kMaxCachedTables = 32;
+
+struct DeviceState {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    int max_smem_optin = 0;
+    int *status = nullptr;  // device: 4 words
+    bool attr_set[8] = {};
+};
+
+std::mutex g_mu;  // guards everything below
+DeviceState g_dev[kMaxDevices];
+
+struct CachedTable {
+    uint64_t key = 0;
+    std::vector<uint8_t> signature;  // exact inputs of the table, to rule out hash collisions
+    void *dev = nullptr;
+    void *host = nullptr;  // pinned copy, kept alive for the asynchronous upload
+    size_t bytes = 0;
+    int device = 0;
+    int grid = 0;
+    int block_n = 0;
+    int stages = 0;
+};
+std::list<CachedTable> g_tables;  // most recently used first
+std::unordered_map<uint64_t, std::list<CachedTable>::iterator> g_table_index;
+
+struct Workspace {
+    void *ptr = nullptr;
+    size_t bytes = 0;
+};
+std::map<std::pair<int, uintptr_t>, Workspace> g_workspaces;  // key: (device, stream)
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+
+int cuda_fail(cudaError_t e)
+{
+    g_last_cuda_error.store((int)e);
+    return NVFP4_ERR_CUDA;
+}
+
+#define CUDA_TRY(call)                          \
+    do {                                        \
+        cudaError_t e_ = (call);                \
+        if (e_ != cudaSuccess)                  \
+            return cuda_fail(e_);               \
+    } while (0)
+
+uint64_t fnv1a(const void *data, size_t n, uint64_t h = 1469598103934665603ull)
+{
+    const uint8_t *p = static_cast<const uint8_t *>(data);
+    for (size_t i = 0; i < n; ++i) {
+        h ^= p[i];
+        h *= 1099511628211ull;
+    }
+    return h;
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Caller holds g_mu.
+int device_state(int dev, DeviceState **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    DeviceState &d = g_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0;
+        CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&d.max_smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        d.supported = (major == 10 && minor == 3);
+        if (d.supported) {
+            CUDA_TRY(cudaMalloc(&d.status, 4 * sizeof(int)));
+            CUDA_TRY(cudaMemset(d.status, 0, 4 * sizeof(int)));
+        }
+        d.ready = true;
+    }
+    if (!d.supported)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return NVFP4_OK;
+}
+
+int get_encoder()
+{
+    if (g_encode)
+        return NVFP4_OK;
+    void *fn = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    CUDA_TRY(cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q));
+    if (q != cudaDriverEntryPointSuccess || !fn)
+        return cuda_fail(cudaErrorNotSupported);
+    g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    return NVFP4_OK;
+}
+
+// A row-major uint8 matrix [rows][row_bytes] read as boxes of 128 bytes x box_rows,
+// with the 128-byte swizzle the MMA's K-major operand layout expects.
+int encode_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {128, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error.store(10000 + (int)r);
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
+int check_problem(const Nvfp4Problem &p)
+{
+    if (p.M < 0 || p.N < 0 || p.K < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (p.sf_layout != NVFP4_SF_PREPACKED && p.sf_layout != NVFP4_SF_ROWMAJOR)
+        return NVFP4_ERR_INVALID_ARG;
+    if (p.M >= kMaxDim || p.N >= kMaxDim || p.K >= kMaxDim)
+        return NVFP4_ERR_TOO_LARGE;
+    if (p.M == 0 || p.N == 0)
+        return NVFP4_OK;
+    if (!p.C)
+        return NVFP4_ERR_INVALID_ARG;
+    if (p.K % 64 != 0 || p.N % 8 != 0 || !aligned16(p.C))
+        return NVFP4_ERR_ALIGNMENT;
+    if (p.K == 0)
+        return NVFP4_OK;
+    if (!p.A || !p.B || !p.SFA || !p.SFB)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(p.A) || !aligned16(p.B) || !aligned16(p.SFA) || !aligned16(p.SFB))
+        return NVFP4_ERR_ALIGNMENT;
+    return NVFP4_OK;
+}
+
+// One active group as the table sees it (scale pointers already blocked).
+struct ActiveGroup {
+    int32_t M, N, K, pad;
+    const void *A, *B, *SFA, *SFB;
+    void *C;
+};
+
+// Per-CTA tile lists. Tiles are numbered group by group, and inside a group
+// B-strip by B-strip (tile_n outer, tile_m inner). Tile t goes to CTA t % grid.
+// So the CTAs that run at the same moment hold consecutive tiles: the m-tiles
+// that share one strip of B read it from HBM once and from L2 after that.
+void build_schedule(const std::vector<ActiveGroup> &gs, int block_n, int grid_cap, std::vector<WorkItem> &items,
+                    std::vector<uint32_t> &cta_begin, int &grid)
+{
+    std::vector<WorkItem> order;
+    for (int gi = 0; gi < (int)gs.size(); ++gi) {
+        const int tm = (gs[gi].M + kBlockM - 1) / kBlockM, tn = (gs[gi].N + block_n - 1) / block_n;
+        for (int n = 0; n < tn; ++n)
+            for (int m = 0; m < tm; ++m)
+                order.push_back(WorkItem{gi, m, n, 0});
+    }
+    grid = std::max(1, std::min<int>((int)order.size(), grid_cap));
+    items.clear();
+    cta_begin.assign(grid + 1, 0);
+    for (int c = 0; c < grid; ++c) {
+        cta_begin[c] = (uint32_t)items.size();
+        for (size_t t = c; t < order.size(); t += grid)
+            items.push_back(order[t]);
+    }
+    cta_begin[grid] = (uint32_t)items.size();
+}
+
+// Caller holds g_mu.
+int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs, int block_n, int stages,
+              int max_ctas, cudaStream_t stream, CachedTable **out)
+{
+    std::vector<uint8_t> sig(sizeof(int) * 4 + gs.size() * sizeof(ActiveGroup));
+    int hdr[4] = {dev, block_n, stages, max_ctas};
+    memcpy(sig.data(), hdr, sizeof(hdr));
+    if (!gs.empty())
+        memcpy(sig.data() + sizeof(hdr), gs.data(), gs.size() * sizeof(ActiveGroup));
+    const uint64_t key = fnv1a(sig.data(), sig.size());
+    auto it = g_table_index.find(key);
+    if (it != g_table_index.end() && it->second->signature == sig) {
+        g_tables.splice(g_tables.begin(), g_tables, it->second);
+        *out = &g_tables.front();
+        return NVFP4_OK;
+    }
+    if (int rc = get_encoder())
+        return rc;
+
+    std::vector<WorkItem> items;
+    std::vector<uint32_t> cta_begin;
+    int grid = 0;
+    const int cap = max_ctas > 0 ? std::min(max_ctas, ds.sm_count) : ds.sm_count;
+    build_schedule(gs, block_n, cap, items, cta_begin, grid);
+
+    const size_t off_groups = sizeof(TableHeader);
+    const size_t off_cta = off_groups + gs.size() * sizeof(GroupEntry);
+    const size_t off_items = (off_cta + (grid + 1) * sizeof(uint32_t) + 15) & ~size_t(15);
+    const size_t total = off_items + items.size() * sizeof(WorkItem);
+
+    CachedTable t;
+    t.key = key;
+    t.signature = std::move(sig);
+    t.bytes = total;
+    t.device = dev;
+    t.grid = grid;
+    t.block_n = block_n;
+    t.stages = stages;
+    CUDA_TRY(cudaMallocHost(&t.host, total));
+    memset(t.host, 0, total);
+    uint8_t *h = static_cast<uint8_t *>(t.host);
+    TableHeader *th = reinterpret_cast<TableHeader *>(h);
+    th->num_groups = (int32_t)gs.size();
+    th->num_items = (int32_t)items.size();
+    th->grid = grid;
+    th->block_n = block_n;
+    th->off_cta_begin = (uint32_t)off_cta;
+    th->off_items = (uint32_t)off_items;
+    th->total_bytes = (uint32_t)total;
+    GroupEntry *ge = reinterpret_cast<GroupEntry *>(h + off_groups);
+    for (size_t i = 0; i < gs.size(); ++i) {
+        const ActiveGroup &a = gs[i];
+        GroupEntry &e = ge[i];
+        int rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, (uint64_t)a.M, kBlockM);
+        if (!rc)
+            rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, (uint32_t)block_n);
+        if (rc) {
+            cudaFreeHost(t.host);
+            return rc;
+        }
+        e.sfa = static_cast<const uint8_t *>(a.SFA);
+        e.sfb = static_cast<const uint8_t *>(a.SFB);
+        e.C = static_cast<__half *>(a.C);
+        e.M = a.M;
+        e.N = a.N;
+        e.K = a.K;
+        e.kblocks64 = a.K / 64;
+        e.tiles_m = (a.M + kBlockM - 1) / kBlockM;
+        e.tiles_n = (a.N + block_n - 1) / block_n;
+    }
+    memcpy(h + off_cta, cta_begin.data(), cta_begin.size() * sizeof(uint32_t));
+    if (!items.empty())
+        memcpy(h + off_items, items.data(), items.size() * sizeof(WorkItem));
+
+    cudaError_t e = cudaMalloc(&t.dev, total);
+    if (e != cudaSuccess) {
+        cudaFreeHost(t.host);
+        return cuda_fail(e);
+    }
+    e = cudaMemcpyAsync(t.dev, t.host, total, cudaMemcpyHostToDevice, stream);
+    if (e != cudaSuccess) {
+        cudaFree(t.dev);
+        cudaFreeHost(t.host);
+        return cuda_fail(e);
+    }
+
+    if (g_tables.size() >= kMaxCachedTables) {
+        // The oldest table may still be read by queued work on any stream.
+        CUDA_TRY(cudaDeviceSynchronize());
+        CachedTable &old = g_tables.back();
+        cudaFree(old.dev);
+        cudaFreeHost(old.host);
+        g_table_index.erase(old.key);
+        g_tables.pop_back();
+    }
+    if (it != g_table_index.end())
+        g_table_index.erase(it);  // a hash collision: the newer table takes the slot
+    g_tables.push_front(std::move(t));
+    g_table_index[key] = g_tables.begin();
+    *out = &g_tables.front();
+    return NVFP4_OK;
+}
+
+template <int BN, int STAGES>
+int launch_gemm(DeviceState &ds, const CachedTable &t, int nslot, cudaStream_t stream, int num_groups)
+{
+    using L = Layout<BN, STAGES>;
+    auto kern = nvfp4_grouped_gemm_kernel<BN, STAGES>;
+    if (L::kSmemBytes > ds.max_smem_optin)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (!ds.attr_set[nslot]) {
+        CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes));
+        ds.attr_set[nslot] = true;
+    }
+    KernelArgs args{};
+    args.table = static_cast<const Table *>(t.dev);
+    args.status = ds.status;
+    args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
+    args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
+    args.num_groups = num_groups;
+    kern<<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
+    CUDA_TRY(cudaGetLastError());
+    return NVFP4_OK;
+}
+
+int workspace_for(int dev, cudaStream_t stream, size_t bytes, void **out)
+{
+    Workspace &w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(stream)}];
+    if (w.bytes < bytes) {
+        if (w.ptr) {
+            CUDA_TRY(cudaStreamSynchronize(stream));
+            cudaFree(w.ptr);
+            w.ptr = nullptr;
+            w.bytes = 0;
+        }
+        const size_t want = std::max(bytes, w.bytes * 2);
+        CUDA_TRY(cudaMalloc(&w.ptr, want));
+        w.bytes = want;
+    }
+    *out = w.ptr;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+// =================================================================== C ABI ==
+
+extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (g < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (g == 0)
+        return NVFP4_OK;
+    if (!probs)
+        return NVFP4_ERR_INVALID_ARG;
+    for (int i = 0; i < g; ++i)
+        if (int rc = check_problem(probs[i]))
+            return rc;
+
+    const int64_t opt_bn = g_opt.block_n.load(), opt_st = g_opt.stages.load();
+    const int block_n = 128;
+    if (opt_bn != 0 && opt_bn != 128)
+        return NVFP4_ERR_INVALID_ARG;
+    const int stages = opt_st == 0 ? 6 : (int)opt_st;
+    if (stages != 2 && stages != 4 && stages != 6)
+        return NVFP4_ERR_INVALID_ARG;
+
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(dev, &ds))
+        return rc;
+
+    // K == 0: C is the empty sum.
+    for (int i = 0; i < g; ++i) {
+        const Nvfp4Problem &p = probs[i];
+        if (p.M > 0 && p.N > 0 && p.K == 0)
+            CUDA_TRY(cudaMemsetAsync(p.C, 0, (size_t)p.M * p.N * sizeof(__half), stream));
+    }
+
+    // Row-major scales go through the prepack kernel into this stream's workspace.
+    std::vector<ActiveGroup> gs;
+    std::vector<PrepackJob> jobs;
+    size_t ws_bytes = 0;
+    std::vector<std::pair<size_t, size_t>> ws_off;  // per active group: SFA, SFB offsets (or SIZE_MAX)
+    for (int i = 0; i < g; ++i) {
+        const Nvfp4Problem &p = probs[i];
+        if (p.M == 0 || p.N == 0 || p.K == 0)
+            continue;
+        gs.push_back(ActiveGroup{p.M, p.N, p.K, 0, p.A, p.B, p.SFA, p.SFB, p.C});
+        if (p.sf_layout == NVFP4_SF_ROWMAJOR) {
+            const size_t oa = ws_bytes;
+            ws_bytes += (blocked_scale_bytes(p.M, p.K / 16) + 255) & ~size_t(255);
+            const size_t ob = ws_bytes;
+            ws_bytes += (blocked_scale_bytes(p.N, p.K / 16) + 255) & ~size_t(255);
+            ws_off.push_back({oa, ob});
+        } else {
+            ws_off.push_back({SIZE_MAX, SIZE_MAX});
+        }
+    }
+    if (gs.empty())
+        return NVFP4_OK;
+    if (ws_bytes > 0) {
+        void *ws = nullptr;
+        if (int rc = workspace_for(dev, stream, ws_bytes, &ws))
+            return rc;
+        uint8_t *base = static_cast<uint8_t *>(ws);
+        for (size_t i = 0; i < gs.size(); ++i) {
+            if (ws_off[i].first == SIZE_MAX)
+                continue;
+            ActiveGroup &a = gs[i];
+            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFA), base + ws_off[i].first, a.M, a.K / 16, 0, 0, 0});
+            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFB), base + ws_off[i].second, a.N, a.K / 16, 0, 0, 0});
+            a.SFA = base + ws_off[i].first;
+            a.SFB = base + ws_off[i].second;
+        }
+        CUDA_TRY(launch_prepack(jobs.data(), (int)jobs.size(), stream));
+    }
+
+    CachedTable *t = nullptr;
+    if (int rc = get_table(dev, *ds, gs, block_n, stages, (int)g_opt.max_ctas.load(), stream, &t))
+        return rc;
+    switch (stages) {
+    case 2: return launch_gemm<128, 2>(*ds, *t, 0, stream, (int)gs.size());
+    case 4: return launch_gemm<128, 4>(*ds, *t, 1, stream, (int)gs.size());
+    default: return launch_gemm<128, 6>(*ds, *t, 2, stream, (int)gs.size());
+    }
+}
+
+extern "C" size_t nvfp4_prepacked_scale_bytes(int rows, int K)
+{
+    if (rows <= 0 || K <= 0)
+        return 0;
+    return (size_t)((rows + 127) / 128) * 128 * (size_t)((K + 63) / 64) * 4;
+}
+
+extern "C" int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, void *sf_blocked, nvfp4_stream_t stream)
+{
+    if (rows < 0 || K < 0 || K % 16 != 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (rows >= kMaxDim || K >= kMaxDim)
+        return NVFP4_ERR_TOO_LARGE;
+    if (rows == 0 || K == 0)
+        return NVFP4_OK;
+    if (!sf_rowmajor || !sf_blocked)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned16(sf_rowmajor) || !aligned16(sf_blocked))
+        return NVFP4_ERR_ALIGNMENT;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int dev = 0;
+        CUDA_TRY(cudaGetDevice(&dev));
+        DeviceState *ds = nullptr;
+        if (int rc = device_state(dev, &ds))
+            return rc;
+    }
+    PrepackJob j{static_cast<const uint8_t *>(sf_rowmajor), static_cast<uint8_t *>(sf_blocked), rows, K / 16, 0, 0, 0};
+    CUDA_TRY(launch_prepack(&j, 1, reinterpret_cast<cudaStream_t>(stream)));
+    return NVFP4_OK;
+}
+
+extern "C" int nvfp4_device_status(nvfp4_stream_t stream, int *status, int32_t *detail)
+{
+    if (!status)
+        return NVFP4_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    DeviceState *ds = nullptr;
+    if (int rc = device_state(dev, &ds))
+        return rc;
+    CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    int words[4] = {0, 0, 0, 0};
+    CUDA_TRY(cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost));
+    if (words[0] != 0)
+        CUDA_TRY(cudaMemset(ds->status, 0, sizeof(words)));
+    *status = words[0];
+    if (detail)
+        for (int i = 0; i < 4; ++i)
+            detail[i] = words[i];
+    return NVFP4_OK;
+}
+
+extern "C" const char *nvfp4_status_string(int code)
+{
+    switch (code) {
+    case NVFP4_OK: return "ok";
+    case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+    case NVFP4_ERR_ALIGNMENT: return "misaligned pointer or size (16-byte pointers, K % 64 == 0, N % 8 == 0)";
+    case NVFP4_ERR_UNSUPPORTED_DEVICE: return "unsupported device (needs compute capability 10.3, sm_103a)";
+    case NVFP4_ERR_CUDA: return "CUDA error (see nvfp4_last_cuda_error)";
+    case NVFP4_ERR_TIMEOUT: return "a kernel wait timed out";
+    case NVFP4_ERR_TOO_LARGE: return "size beyond the library's limits";
+    default: return "unknown status";
+    }
+}
+
+extern "C" int nvfp4_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+extern "C" int nvfp4_set_option(int option, int64_t value)
+{
+    switch (option) {
+    case NVFP4_OPT_BLOCK_N:
+        if (value != 0 && value != 128)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.block_n = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_STAGES:
+        if (value != 0 && value != 2 && value != 4 && value != 6)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.stages = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_MAX_CTAS:
+        if (value < 0)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.max_ctas = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_WAIT_TIMEOUT_US:
+        if (value < 1 || value > 60000000)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.timeout_us = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_FAULT_SKIP_LOAD:
+        if (value < -1)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.fault_skip_load = value;
+        return NVFP4_OK;
+    default:
+        return NVFP4_ERR_INVALID_ARG;
+    }
+}
+
+extern "C" void nvfp4_release(void)
+{
+    std::lock_guard<std::mutex> lock(g_mu);
+    int cur = 0;
+    if (cudaGetDevice(&cur) != cudaSuccess)
+        cur = -1;
+    for (int d = 0; d < kMaxDevices; ++d) {
+        if (!g_dev[d].ready)
+            continue;
+        cudaSetDevice(d);
+        cudaDeviceSynchronize();
+        for (auto it = g_tables.begin(); it != g_tables.end();) {
+            if (it->device == d) {
+                cudaFree(it->dev);
+                cudaFreeHost(it->host);
+                g_table_index.erase(it->key);
+                it = g_tables.erase(it);
+            } else {
+                ++it;
+            }
+        }
+        for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
+            if (it->first.first == d) {
+                cudaFree(it->second.ptr);
+                it = g_workspaces.erase(it);
+            } else {
+                ++it;
+            }
+        }
+        if (g_dev[d].status)
+            cudaFree(g_dev[d].status);
+        g_dev[d] = DeviceState{};
+    }
+    if (cur >= 0)
+        cudaSetDevice(cur);
+}

@@ -1,0 +1,163 @@
+/*
+ * nvfp4_grouped_gemm.h -- C ABI of the grouped NVFP4 block-scaled GEMM library
+ * (libnvfp4gg.so, built for sm_103a).
+ *
+ * The operation, for each group i < g (one kernel launch for all groups):
+ *
+ *   C_i[m][n] = fp16( sum_k e2m1(A_i[m][k]) * e4m3(SFA_i[m][k/16])
+ *                          * e2m1(B_i[n][k]) * e4m3(SFB_i[n][k/16]) )
+ *
+ * Sources:
+ *  - page 3 (kernelindex.com submission 444497), kernel header comment:
+ *    C[i](M_i x N_i) = A[i](M_i x K_i) . B[i](N_i x K_i)^T, with E2M1 data,
+ *    E4M3FN scales and fp16 output;
+ *  - page 2 (submission 505431), python section, `custom_kernel_fallback`:
+ *    dequantise, multiply each 16-element block by its scale, take the
+ *    product in fp32 and cast to fp16.
+ * The tensor cores add the products in fp32, so the result is one of the
+ * fp16 values near the exact sum. It agrees with the exact result within
+ * 1e-3 * sum_k |a*sa*b*sb| + 1 fp16 ulp.
+ *
+ * All pointers in Nvfp4Problem are DEVICE pointers on the current CUDA device.
+ * The caller owns every buffer and the stream. Every call is stream-ordered and
+ * asynchronous: it never synchronises the stream, and the inputs must stay
+ * valid until the stream has run the launched work.
+ *
+ * Return codes: NVFP4_OK (0) or a negative NVFP4_ERR_* value. Arguments are
+ * checked on the host before anything is queued. When a check fails, nothing
+ * is launched.
+ */
+#ifndef NVFP4_GROUPED_GEMM_H
+#define NVFP4_GROUPED_GEMM_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* The same type as cudaStream_t. NULL means the legacy default stream. */
+typedef struct CUstream_st *nvfp4_stream_t;
+
+enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = -1,        /* g < 0, NULL probs, negative sizes, NULL pointer of a non-empty operand, bad sf_layout */
+    NVFP4_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, K % 64 != 0, or N % 8 != 0 */
+    NVFP4_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 (sm_103a) */
+    NVFP4_ERR_CUDA = -4,               /* a CUDA runtime or driver call failed; see nvfp4_last_cuda_error() */
+    NVFP4_ERR_TIMEOUT = -5,            /* a kernel gave up a bounded wait; reported by nvfp4_device_status() */
+    NVFP4_ERR_TOO_LARGE = -6           /* a size beyond the library's limits (e.g. M, N or K >= 2^24) */
+};
+
+/* Scale-factor layouts of SFA/SFB. */
+enum {
+    /* The 128 x 4 blocked layout: see nvfp4_prepack_scales(). This is the layout
+     * the kernel reads. */
+    NVFP4_SF_PREPACKED = 0,
+    /* Row-major [rows][K/16]. The call first runs the prepack kernel into a
+     * library-owned workspace (one extra launch), then the GEMM. */
+    NVFP4_SF_ROWMAJOR = 1
+};
+
+/* One GEMM of the group.
+ *  M, N, K  : sizes. M, N >= 0; K >= 0 with K % 64 == 0 (the MMA consumes K in
+ *             steps of 64); N % 8 == 0 (16-byte rows of C); each < 2^24.
+ *             M == 0 or N == 0 leaves the group out. K == 0 writes C = 0.
+ *  A        : [M][K/2] bytes, row-major. Byte j of a row holds element 2j in its
+ *             low nibble and element 2j+1 in its high nibble (page 2, python
+ *             section, `dequantize_fp4`). E2M1 code: sign bit 3, magnitude
+ *             0, .5, 1, 1.5, 2, 3, 4, 6 for codes 0..7.
+ *  B        : [N][K/2] bytes, the same packing. B is N x K, and C = A . B^T.
+ *  SFA, SFB : E4M3 scale bytes, one per 16 consecutive K of a row, in the layout
+ *             sf_layout names. The scale type the tensor core reads is unsigned
+ *             (UE4M3), so the sign bit must be 0. 0x7F is NaN and not allowed.
+ *  C        : [M][N] fp16, row-major, ldc = N. Only m < M and n < N are written.
+ *  A, B, SFA, SFB and C must be 16-byte aligned. */
+typedef struct {
+    int32_t M, N, K;
+    int32_t sf_layout;
+    const void *A;
+    const void *B;
+    const void *SFA;
+    const void *SFB;
+    void *C;
+} Nvfp4Problem;
+
+/* The grouped GEMM: one persistent kernel launch for all g problems (plus a
+ * prepack launch when some scales are row-major, plus a memset per K == 0
+ * group).
+ *
+ * probs is read during the call only. The library keeps, per distinct problem
+ * set, a device-side table: tensor maps, per-group pointers and the tile
+ * schedule. The table is cached by a hash of probs, so a repeated call
+ * uploads nothing.
+ *
+ * g == 0 is a no-op and returns NVFP4_OK. Errors: see the enum above. A
+ * timeout inside the kernel is reported only by nvfp4_device_status(). */
+int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream_t stream);
+
+/* Size in bytes of the blocked scale layout for a rows x K operand:
+ * 128*ceil(rows/128) * 4*ceil(K/64). Returns 0 when rows <= 0 or K <= 0. */
+size_t nvfp4_prepacked_scale_bytes(int rows, int K);
+
+/* Scale prepack: row-major [rows][K/16] E4M3 bytes -> the 128 x 4 blocked layout
+ * that the tensor core's scale copy reads. Page 4 (submission 482006),
+ * `to_blocked_gpu`, defines the layout. Pad the rows to a multiple of 128 and
+ * the scale columns to a multiple of 4 with zeros. Cut the result into 512-byte
+ * blocks, one per (128-row tile, 4 scale columns). Blocks are ordered
+ * row-tile major, with K blocks inner. Inside a block, row r = 32*i + j and
+ * column c land at byte j*16 + i*4 + c.
+ *  sf_rowmajor : device, rows*(K/16) bytes.
+ *  sf_blocked  : device, nvfp4_prepacked_scale_bytes(rows, K) bytes, written
+ *                in full, padding included.
+ *  K % 16 == 0. Both pointers 16-byte aligned. One launch, stream-ordered.
+ *  rows == 0 or K == 0 is a no-op. */
+int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, void *sf_blocked, nvfp4_stream_t stream);
+
+/* Reads and clears the current device's error word, which kernels set when a
+ * bounded wait runs out. Synchronises `stream` first.
+ *  *status = NVFP4_OK, or NVFP4_ERR_TIMEOUT if any launch since the last read
+ *  gave up a wait.
+ *  detail (may be NULL) receives 4 words: the code, the role (0 producer,
+ *  1 MMA, 2 epilogue, 3 teardown), the work item and the k-stage at which the
+ *  first timeout happened.
+ * Returns NVFP4_OK or an NVFP4_ERR_* code of its own. */
+int nvfp4_device_status(nvfp4_stream_t stream, int *status, int32_t *detail);
+
+/* A static, human-readable name for a return code. */
+const char *nvfp4_status_string(int code);
+
+/* The cudaError_t value of the last failed CUDA call (0 if none). */
+int nvfp4_last_cuda_error(void);
+
+/* Options for tests and tuning. They apply to the calls that follow, are
+ * process-wide, and take part in the table cache's key.
+ *  NVFP4_OPT_BLOCK_N       : 0 = automatic, or 128
+ *  NVFP4_OPT_STAGES        : 0 = automatic, or 2..6 (shared-memory ring depth)
+ *  NVFP4_OPT_MAX_CTAS      : 0 = one per SM, or an upper bound on the grid
+ *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
+ *                             (default 2,000,000 us)
+ *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
+ *                             CTA 0 skips the copies of its k-stage with that
+ *                             global index. The consumer's wait then runs out
+ *                             and the kernel reports NVFP4_ERR_TIMEOUT instead
+ *                             of hanging. Only for testing the timeout path.
+ * Returns NVFP4_OK or NVFP4_ERR_INVALID_ARG. */
+enum {
+    NVFP4_OPT_BLOCK_N = 1,
+    NVFP4_OPT_STAGES = 2,
+    NVFP4_OPT_MAX_CTAS = 3,
+    NVFP4_OPT_WAIT_TIMEOUT_US = 4,
+    NVFP4_OPT_FAULT_SKIP_LOAD = 5
+};
+int nvfp4_set_option(int option, int64_t value);
+
+/* Frees every cached table and workspace of every device. Synchronises each
+ * device that holds one. Calls made afterwards start again from empty caches. */
+void nvfp4_release(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_GROUPED_GEMM_H */

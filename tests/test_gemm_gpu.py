@@ -1,0 +1,190 @@
+"""Parity of the CUDA path with the CPU oracle, through the C ABI.
+
+Bars:
+ * scale prepack: byte-for-byte identical to the oracle's blocked layout;
+ * GEMM: every compared output within |C_gpu - C_oracle| <= 1e-3 * S + 1 ulp16;
+ * no store outside C (4 KB canary bands on both sides) and no output left unwritten;
+ * results independent of the pipeline depth and of the number of CTAs, bit for bit.
+Small workloads compare every output. The full-size workloads run in the launch
+configuration the benchmark uses and compare sampled outputs, computed one by
+one by the oracle.
+"""
+import numpy as np
+import pytest
+import torch
+
+import gen
+import oracle
+from parity import assert_within_bound
+import block_scaled_fp4_persistent_gb300 as nv
+from gpu_util import DeviceGroup, run
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True)
+def _defaults():
+    yield
+    for opt, val in [(nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_BLOCK_N, 0),
+                     (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000)]:
+        nv.nvfp4_set_option(opt, val)
+
+
+def check_full(groups, dgroups, what):
+    ref = oracle.grouped_gemm(groups)
+    for i, ((c_ref, s_ref), d) in enumerate(zip(ref, dgroups)):
+        got = d.result()
+        assert not np.isnan(got).any(), f"{what} group {i}: unwritten outputs"
+        assert_within_bound(got, c_ref, s_ref, f"{what} group {i}")
+        assert d.guards_intact(), f"{what} group {i}: store outside C"
+
+
+# ------------------------------------------------------------------ prepack --
+
+@pytest.mark.parametrize("rows,K", [(1, 64), (40, 2048), (128, 256), (129, 320), (300, 1024), (248, 7168),
+                                    (7, 48), (4096, 1536)])
+def test_prepack_bitwise(rows, K):
+    rng = np.random.default_rng(rows + K)
+    sf = rng.integers(0, 256, (rows, K // 16), dtype=np.uint8)
+    out = nv.prepack_scales(torch.from_numpy(sf).cuda(), K)
+    torch.cuda.synchronize()
+    ref = oracle.blocked_scales(sf)
+    assert np.array_equal(out.cpu().numpy()[:ref.size], ref)
+
+
+# ------------------------------------------------------------ small, full ---
+
+def test_tiny_workload_every_output():
+    groups = gen.make_workload("tiny_g2")
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    check_full(groups, d, "tiny_g2")
+
+
+RAGGED = dict(seed=77, Ms=[1, 40, 127, 128, 129, 248, 300], Ns=[8, 120, 136, 512, 264, 128, 72],
+              Ks=[64, 192, 256, 320, 1024, 512, 2304])
+
+
+@pytest.mark.parametrize("layout", [nv.NVFP4_SF_PREPACKED, nv.NVFP4_SF_ROWMAJOR])
+def test_ragged_shapes_one_launch(layout):
+    groups = gen.make_problem_set(RAGGED["seed"], RAGGED["Ms"], RAGGED["Ns"], RAGGED["Ks"])
+    d = [DeviceGroup(g, layout) for g in groups]
+    run(d)
+    check_full(groups, d, f"ragged layout={layout}")
+
+
+def test_structured_closed_form():
+    # all elements 1.0 with scales 0.5 and 2 (codes 0x30, 0x40): C = K exactly
+    class G:
+        pass
+    groups = []
+    for M, N, K in [(130, 200, 2048), (5, 8, 64)]:
+        g = G()
+        g.M, g.N, g.K = M, N, K
+        g.A = np.full((M, K // 2), 0x22, np.uint8)
+        g.B = np.full((N, K // 2), 0x22, np.uint8)
+        g.SFA = np.full((M, K // 16), 0x30, np.uint8)
+        g.SFB = np.full((N, K // 16), 0x40, np.uint8)
+        groups.append(g)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    for g, dg in zip(groups, d):
+        assert np.all(dg.result().astype(np.float64) == g.K)
+
+
+@pytest.mark.parametrize("stages", [2, 4, 6])
+@pytest.mark.parametrize("max_ctas", [1, 3, 0])
+def test_pipeline_depth_and_grid_do_not_change_results(stages, max_ctas):
+    groups = gen.make_problem_set(5, [200, 64, 129], [384, 256, 136], [1536, 512, 768])
+    base = [DeviceGroup(g) for g in groups]
+    run(base)
+    check_full(groups, base, "baseline") if (stages, max_ctas) == (6, 0) else None
+    nv.nvfp4_set_option(nv.NVFP4_OPT_STAGES, stages)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, max_ctas)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    for a, b in zip(base, d):
+        assert np.array_equal(a.result().view(np.uint16), b.result().view(np.uint16))
+        assert b.guards_intact()
+
+
+# --------------------------------------------------------------- edge cases ---
+
+def test_edge_cases_empty_groups_and_k0():
+    groups = gen.make_problem_set(9, [0, 64, 3, 0, 130], [64, 0, 16, 8, 256], [256, 256, 0, 0, 128])
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    assert np.all(d[2].result() == 0)  # K = 0: the empty sum
+    assert d[2].guards_intact()
+    check_full([groups[4]], [d[4]], "after empties")
+    nv.nvfp4_grouped_gemm([])  # g = 0
+
+
+def test_repeated_calls_and_table_cache():
+    ga = gen.make_problem_set(13, [96, 160], [256, 128], [512, 256])
+    gb = gen.make_problem_set(14, [33], [64], [1024])
+    da = [DeviceGroup(g) for g in ga]
+    db = [DeviceGroup(g) for g in gb]
+    run(da)
+    first = [x.result().copy() for x in da]
+    run(db)
+    for x in da:
+        x.reset()
+    run(da)  # table cache hit
+    for f, x in zip(first, da):
+        assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
+    check_full(gb, db, "second problem set")
+
+
+def test_many_groups():
+    rng = np.random.default_rng(3)
+    Ms = [int(m) for m in rng.integers(1, 300, 40)]
+    Ns = [int(n) * 8 for n in rng.integers(1, 48, 40)]
+    Ks = [int(k) * 64 for k in rng.integers(1, 12, 40)]
+    groups = gen.make_problem_set(17, Ms, Ns, Ks)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    check_full(groups, d, "40 groups")
+
+
+def test_streams_are_respected():
+    groups = gen.make_problem_set(21, [128, 64], [512, 256], [1024, 512])
+    d = [DeviceGroup(g) for g in groups]
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):
+        nv.nvfp4_grouped_gemm([x.problem() for x in d], s)
+    s.synchronize()
+    status, _ = nv.nvfp4_device_status(s)
+    assert status == 0
+    check_full(groups, d, "side stream")
+
+
+# --------------------------------------------------------- full-size, sampled ---
+
+def sample_indices(M, N, n, rng):
+    ms = list(rng.integers(0, M, n)) + [0, M - 1, 0, M - 1] + [M - 1] * 8 + list(range(min(M, 8)))
+    ns = list(rng.integers(0, N, n)) + [0, 0, N - 1, N - 1] + list(rng.integers(0, N, 8)) + [N - 1] * min(M, 8)
+    return np.array(ms), np.array(ns)
+
+
+@pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
+def test_full_size_workloads_sampled(name):
+    groups = gen.make_workload(name)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)  # default options: the launch configuration of the benchmark
+    rng = np.random.default_rng(99)
+    again = None
+    for i, (g, x) in enumerate(zip(groups, d)):
+        got = x.result()
+        assert not np.isnan(got).any(), f"{name} group {i}: unwritten outputs"
+        assert x.guards_intact()
+        ms, ns = sample_indices(g.M, g.N, 3000, rng)
+        c_ref, s_ref = oracle.gemm_entries(g, ms, ns)
+        assert_within_bound(got[ms, ns], c_ref, s_ref, f"{name} group {i}")
+    # a property that holds at any size: a second launch gives the same bits
+    first = [x.result().copy() for x in d]
+    for x in d:
+        x.reset()
+    run(d)
+    for f, x in zip(first, d):
+        assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
