@@ -1,0 +1,480 @@
+#!/usr/bin/env python3
+"""Benchmark of the grouped NVFP4 block-scaled GEMM (one JSON line on stdout).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+Metric: microseconds per grouped call. Also reported: effective TFLOP/s and
+TB/s, and the fraction of the roofline max(2*sum(M*N*K) / FP4 peak,
+algorithmic bytes / HBM peak).
+
+The default workload is the MoE-shaped g=8 problem with M = 80,176,128,72,64,248,96,160,
+N = 4096 and K = 7168 (seed 1111). It is the largest of the leaderboard shapes and the
+first line of the timing table on page 1 of the pages. The inputs are synthetic, from
+`gen` (SplitMix64): uniform E2M1 nibbles, and E4M3 scales uniform over
+the codes 0x20..0x40.
+
+Timing (ours):
+ * Inputs are resident in HBM, with scales prepacked. Warm-up calls run first,
+   and the device table is cached by then.
+ * Before every timed call, L2 is flushed: a 2 x L2 buffer is written, then a
+   second 2 x L2 buffer is read, so that the call starts with an L2 holding
+   neither its inputs nor dirty lines.
+ * Each call is timed alone with CUDA events on the launching stream.
+   `value` is the mean over K calls; median, min and max are also reported.
+ * e2e runs the same call through the public API from pinned HOST buffers with
+   row-major scales. Each timed step copies A, B, SFA and SFB host->device,
+   runs the prepack and the GEMM, and copies C device->host.
+ * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
+   scaling; the path has no exchange step). Timing is the max over ranks, and
+   `value` = that time divided by N (aggregate time per grouped call).
+--impl reference times the CPU oracle (the plain C reference restated from the
+pages) on bounded samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import gen  # noqa: E402
+
+NOMINAL_BF16_TFLOPS = 2250.0
+NOMINAL_FP4_TFLOPS = 13500.0  # dense NVFP4, GB300
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+GEMM_KERNEL_NAME = "nvfp4_grouped_gemm_kernel"
+KERNEL_SOURCES = ["block_scaled_fp4_persistent_gb300/csrc/gemm_kernel.cuh",
+                  "block_scaled_fp4_persistent_gb300/csrc/ptx.cuh",
+                  "block_scaled_fp4_persistent_gb300/csrc/table.h"]
+
+
+# ------------------------------------------------------------------ helpers --
+
+def workload_stats(groups):
+    flops = sum(2 * g.M * g.N * g.K for g in groups)
+    nbytes = sum(g.M * g.K // 2 + g.N * g.K // 2 + g.M * g.K // 16 + g.N * g.K // 16 + 2 * g.M * g.N for g in groups)
+    return flops, nbytes
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            p = json.load(f)
+        return p, "measured"
+    return dict(FALLBACK_PEAKS), "fallback"
+
+
+def roofline_terms(groups, peaks):
+    flops, nbytes = workload_stats(groups)
+    fp4_tflops = peaks["bf16_tflops"] * NOMINAL_FP4_TFLOPS / NOMINAL_BF16_TFLOPS
+    t_fp4_us = flops / (fp4_tflops * 1e12) * 1e6
+    t_hbm_us = nbytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    return flops, nbytes, fp4_tflops, t_fp4_us, t_hbm_us
+
+
+def kernel_source_hash():
+    h = hashlib.sha256()
+    for rel in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def profiled_traffic(workload):
+    """dram read+write bytes per launch from the committed ncu summary of this
+    workload, or None when that summary was taken on other kernel sources."""
+    path = os.path.join(ROOT, "profiles", f"{GEMM_KERNEL_NAME}_{workload}.txt")
+    if not os.path.exists(path):
+        return None
+    fields = {}
+    for line in open(path):
+        if ":" in line and not line.startswith(" "):
+            k, v = line.split(":", 1)
+            fields[k.strip()] = v.strip()
+    if fields.get("kernel_sources_sha256_16") != kernel_source_hash():
+        return None
+    try:
+        return float(fields["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples every 200 ms while running."""
+
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except OSError:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.thread.join(timeout=2)
+
+    def summary(self):
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# --------------------------------------------------------- distributed glue --
+
+def dist_env():
+    return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), int(os.environ.get("LOCAL_RANK", "0"))
+
+
+def reduce_max(value: float, world: int):
+    """Max of `value` over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = torch.device("cuda", torch.cuda.current_device()) if dist.get_backend() == "nccl" else torch.device("cpu")
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ------------------------------------------------------------- CPU oracle leg --
+
+def _row_slices(groups, start, count):
+    """`count` output rows taken cyclically from row `start` of the concatenation of all groups'
+    rows, as sub-groups (consecutive rows of one group stay together)."""
+    total = sum(g.M for g in groups)
+    offs = np.cumsum([0] + [g.M for g in groups])
+    picked = {}
+    for j in range(min(count, total)):
+        r = (start + j) % total
+        gi = int(np.searchsorted(offs, r, side="right") - 1)
+        picked.setdefault(gi, []).append(r - int(offs[gi]))
+    sub = []
+    for gi, rows in picked.items():
+        g = groups[gi]
+        idx = np.array(sorted(rows))
+        sub.append(gen.GroupInputs(len(idx), g.N, g.K, g.A[idx], g.B, g.SFA[idx], g.SFB))
+    return sub
+
+
+def oracle_sample(groups, start, rows, threads):
+    """Runs the oracle on `rows` output rows. Returns (seconds, multiply-adds, threads used)."""
+    import oracle
+    sub = _row_slices(groups, start, rows)
+    t0 = time.perf_counter()
+    oracle.grouped_gemm(sub, nthreads=threads)
+    dt = time.perf_counter() - t0
+    return dt, sum(g.M * g.N * g.K for g in sub), min(threads, max(g.M for g in sub))
+
+
+def oracle_rows_for(groups, budget_s, threads):
+    """How many rows one sample may take to stay near budget_s (at least 1)."""
+    dt, _, _ = oracle_sample(groups, 0, 1, threads)
+    waves = int(budget_s / max(dt, 1e-4))
+    rows = max(1, threads * waves) if waves >= 1 else 1
+    return min(rows, sum(g.M for g in groups))
+
+
+def time_oracle(groups, target_s, threads):
+    """The oracle on a row sample sized to about target_s seconds, scaled to one full grouped
+    call by multiply-adds. Returns (us per call, sample description, threads used)."""
+    rows = oracle_rows_for(groups, target_s, threads)
+    dt, macs, used = oracle_sample(groups, 0, rows, threads)
+    macs_full = sum(g.M * g.N * g.K for g in groups)
+    desc = (f"{min(rows, sum(g.M for g in groups))} of {sum(g.M for g in groups)} output rows (all N, all K), "
+            f"{dt:.2f} s; time scaled by full/sampled multiply-adds")
+    return dt * 1e6 * macs_full / macs, desc, used
+
+
+# ---------------------------------------------------------------- our arm ---
+
+def run_ours(args, groups, rank, world, local_rank):
+    import torch
+    import block_scaled_fp4_persistent_gb300 as nv
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    peaks, peak_kind = load_peaks()
+    flops, nbytes, fp4_tflops, t_fp4_us, t_hbm_us = roofline_terms(groups, peaks)
+
+    # inputs resident in HBM, scales prepacked
+    keep, probs = [], []
+    for g in groups:
+        A = torch.from_numpy(g.A).to(dev)
+        B = torch.from_numpy(g.B).to(dev)
+        SFA = nv.prepack_scales(torch.from_numpy(g.SFA).to(dev), g.K)
+        SFB = nv.prepack_scales(torch.from_numpy(g.SFB).to(dev), g.K)
+        C = torch.empty((g.M, g.N), dtype=torch.float16, device=dev)
+        keep.append((A, B, SFA, SFB, C))
+        probs.append(nv.problem(A, B, SFA, SFB, C))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.fill_(1.0)
+        torch.sum(flush_r, dim=(0,), keepdim=True, out=sink)
+
+    for _ in range(args.warmup):
+        flush()
+        nv.nvfp4_grouped_gemm(probs, stream)
+    torch.cuda.synchronize()
+    st, detail = nv.nvfp4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    fl_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    with ClockSampler(local_rank) as clocks:
+        barrier(world)
+        torch.cuda.synchronize()
+        w0 = time.perf_counter()
+        for i in range(args.steps):
+            fl_starts[i].record(stream)
+            flush()
+            starts[i].record(stream)
+            nv.nvfp4_grouped_gemm(probs, stream)
+            ends[i].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+        wall = time.perf_counter() - w0
+    st, detail = nv.nvfp4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+    per_call_ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    flush_ms = [s.elapsed_time(e) for s, e in zip(fl_starts, starts)]
+    mean_us = statistics.fmean(per_call_ms) * 1e3
+    med_us = statistics.median(per_call_ms) * 1e3
+    mean_us_all = reduce_max(mean_us, world)
+
+    # end to end: host buffers, row-major scales, copies inside the timed region
+    e2e_steps = max(1, min(args.steps, args.e2e_steps))
+    hostbufs, dbufs, e2e_probs = [], [], []
+    h2d = d2h = 0
+    for g in groups:
+        hA = torch.from_numpy(g.A).pin_memory()
+        hB = torch.from_numpy(g.B).pin_memory()
+        hSFA = torch.from_numpy(g.SFA).pin_memory()
+        hSFB = torch.from_numpy(g.SFB).pin_memory()
+        hC = torch.empty((g.M, g.N), dtype=torch.float16).pin_memory()
+        dA, dB = torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev)
+        dSFA, dSFB = torch.empty_like(hSFA, device=dev), torch.empty_like(hSFB, device=dev)
+        dC = torch.empty((g.M, g.N), dtype=torch.float16, device=dev)
+        hostbufs.append((hA, hB, hSFA, hSFB, hC))
+        dbufs.append((dA, dB, dSFA, dSFB, dC))
+        e2e_probs.append(nv.problem(dA, dB, dSFA, dSFB, dC, nv.NVFP4_SF_ROWMAJOR))
+        h2d += sum(t.numel() * t.element_size() for t in (hA, hB, hSFA, hSFB))
+        d2h += hC.numel() * hC.element_size()
+
+    def e2e_step():
+        for (hA, hB, hSFA, hSFB, _), (dA, dB, dSFA, dSFB, _) in zip(hostbufs, dbufs):
+            dA.copy_(hA, non_blocking=True)
+            dB.copy_(hB, non_blocking=True)
+            dSFA.copy_(hSFA, non_blocking=True)
+            dSFB.copy_(hSFB, non_blocking=True)
+        nv.nvfp4_grouped_gemm(e2e_probs, stream)
+        for (*_, hC), (*_, dC) in zip(hostbufs, dbufs):
+            hC.copy_(dC, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    e2e_us = reduce_max(e0.elapsed_time(e1) * 1e3 / e2e_steps, world)
+    st, detail = nv.nvfp4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+    # the e2e result must match the resident-input result bit for bit
+    for (_, _, _, _, C), (*_, hC) in zip(keep, hostbufs):
+        if not torch.equal(C.cpu().view(torch.int16), hC.view(torch.int16)):
+            raise RuntimeError("e2e output differs from the resident-input output")
+
+    achieved_gbs = nbytes / (mean_us * 1e-6) / 1e9
+    roof_us = max(t_fp4_us, t_hbm_us)
+    out = {
+        "metric": "us per grouped call (NVFP4 block-scaled grouped GEMM, fp16 out)",
+        "value": round(mean_us_all / world, 3),
+        "unit": "us",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(mean_us_all / 1e3, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "e2m1 x e2m1 (ue4m3 block-16 scales), fp32 accumulate, fp16 out",
+        "data": "synthetic (SplitMix64 seeded generator; shapes and distributions of the leaderboard workload)",
+        "config": {"workload": args.workload, "g": len(groups), "M": [g.M for g in groups],
+                   "N": [g.N for g in groups], "K": [g.K for g in groups], "seed": gen.WORKLOADS[args.workload]["seed"],
+                   "scales": "prepacked 128x4 blocked layout", "l2": "flushed before every timed call "
+                   "(2xL2 write, then 2xL2 read)", "parallelism": f"replicas x{world}"},
+        "median_us": round(med_us, 3),
+        "min_us": round(min(per_call_ms) * 1e3, 3),
+        "max_us": round(max(per_call_ms) * 1e3, 3),
+        "tflops": round(flops / (mean_us * 1e-6) / 1e12, 2),
+        "tbs": round(achieved_gbs / 1e3, 4),
+        "roofline_us": round(roof_us, 3),
+        "roofline_fraction": round(roof_us / mean_us, 4),
+        "roofline_terms_us": {"fp4": round(t_fp4_us, 3), "hbm": round(t_hbm_us, 3),
+                              "fp4_peak_tflops": round(fp4_tflops, 1),
+                              "fp4_peak_kind": f"{peak_kind} bf16 x nominal fp4/bf16 ratio 6"},
+        "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} (copy bandwidth)",
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": profiled_traffic(args.workload),
+                     "kernel": GEMM_KERNEL_NAME},
+        "gpu_launches": args.steps,
+        "time_share": {"gemm": round(sum(per_call_ms) / (sum(per_call_ms) + sum(flush_ms)), 4),
+                       "l2_flush": round(sum(flush_ms) / (sum(per_call_ms) + sum(flush_ms)), 4)},
+        "timed_region_wall_s": round(wall, 3),
+        "clocks": clocks.summary(),
+        "e2e": {"value": round(e2e_us / world, 3), "unit": "us", "steps": e2e_steps, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "gpu_launches_per_step": 2,
+                "path": "pinned host A/B/row-major SFA/SFB -> H2D -> nvfp4_grouped_gemm (prepack + GEMM) -> D2H C"},
+    }
+    return out
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10000)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="moe_g8_n4096_k7168", choices=sorted(gen.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=100)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle timing sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local_rank = dist_env()
+    if world != args.gpus:
+        if world == 1 and args.gpus > 1:
+            ap.error("--gpus > 1 needs torchrun (one process per GPU)")
+    w = gen.WORKLOADS[args.workload]
+
+    if args.impl == "reference":
+        if rank != 0:
+            return 0
+        groups = gen.make_problem_set(w["seed"], w["Ms"], w["Ns"], w["Ks"])
+        threads = os.cpu_count() or 1
+        flops, nbytes = workload_stats(groups)
+        macs_full = flops // 2
+        budget = max(0.02, 90.0 / (args.steps + args.warmup))
+        rows = oracle_rows_for(groups, budget, threads)
+        cursor = 0
+        for _ in range(args.warmup):
+            oracle_sample(groups, cursor, rows, threads)
+            cursor += rows
+        samples, used = [], 1
+        for _ in range(args.steps):
+            dt, macs, used = oracle_sample(groups, cursor, rows, threads)
+            cursor += rows
+            samples.append(dt * 1e6 * macs_full / macs)
+        desc = (f"each step: {rows} consecutive output rows (all N, all K) of the {sum(w['Ms'])} in one call, "
+                f"cycling through the groups; time scaled by full/sampled multiply-adds")
+        value = statistics.fmean(samples)
+        print(json.dumps({
+            "impl": "reference", "metric": "us per grouped call (NVFP4 block-scaled grouped GEMM, fp16 out)",
+            "value": round(value, 1), "unit": "us", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(value / 1e3, 3), "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+            "dtype": "f64 accumulate, fp16 out", "data": "synthetic",
+            "config": {"workload": args.workload, "g": len(groups), "M": w["Ms"], "N": w["Ns"], "K": w["Ks"],
+                       "seed": w["seed"]},
+            "tflops": round(flops / (value * 1e-6) / 1e12, 6), "tbs": round(nbytes / (value * 1e-6) / 1e12, 6),
+            "cpu_baseline": {"value": round(value, 1), "unit": "us", "cores": used, "kind": "oracle",
+                             "sample": desc},
+            "e2e": {"value": round(value, 1), "unit": "us", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        }))
+        return 0
+
+    if world > 1:
+        import torch
+        import torch.distributed as dist
+        torch.cuda.set_device(local_rank)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    # each rank draws its own replica of the workload (weak scaling)
+    groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
+    out = run_ours(args, groups, rank, world, local_rank)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            threads = os.cpu_count() or 1
+            us, desc, used = time_oracle(groups, args.cpu_seconds, threads)
+            out["cpu_baseline"] = {"value": round(us, 1), "unit": "us", "cores": used, "kind": "oracle",
+                                   "sample": desc}
+        print(json.dumps(out))
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+if __name__ == "__main__":
+    sys.exit(main())
