@@ -180,3 +180,15 @@ def prepack_scales(sf_rowmajor, K: int, out=None, stream=None):
         out = torch.empty(max(1, nvfp4_prepacked_scale_bytes(rows, K)), dtype=torch.uint8, device=sf_rowmajor.device)
     nvfp4_prepack_scales(sf_rowmajor.data_ptr(), rows, K, out.data_ptr(), stream)
     return out
+
+
+def nvfp4_grouped_gemm_noalloc(probs: Sequence[Nvfp4Problem], stream=None, check: bool = True) -> int:
+    """The grouped GEMM without any device allocation: its problem table lives in a
+    fixed 256 KB array inside the library (see the C header for the limits)."""
+    lib_ = _get()
+    fn = lib_.nvfp4_grouped_gemm_noalloc
+    fn.restype = ctypes.c_int
+    fn.argtypes = [ctypes.c_int, ctypes.POINTER(Nvfp4Problem), ctypes.c_void_p]
+    arr = (Nvfp4Problem * max(1, len(probs)))(*probs)
+    rc = fn(len(probs), arr, _stream_handle(stream))
+    return _check(rc, "nvfp4_grouped_gemm_noalloc") if check else rc

@@ -591,3 +591,202 @@ extern "C" void nvfp4_release(void)
     if (cur >= 0)
         cudaSetDevice(cur);
 }
+
+// ======================================================= no-allocation entry ==
+//
+// nvfp4_grouped_gemm_noalloc: the same grouped GEMM kernel for callers that
+// cannot allocate device memory. Examples: code running inside a custom
+// allocator or an out-of-memory handler, or a runtime that owns every byte of
+// device memory and forbids cudaMalloc/cudaFree from libraries. The caller
+// still passes A, B, SFA, SFB and C. The kernel's only other device memory (its
+// problem table and its error words) lives in the fixed array below, which is
+// part of the loaded module. Every GPU that loads this library holds this
+// array until the process exits.
+//
+// Limits and rules (repeated in the header):
+//  * Scratch size kNoAllocScratchBytes (256 KB). The first 256 bytes hold the
+//    error words and the rest holds the table:
+//    128 + sizeof(GroupEntry) * g + 4 * (grid + 1) (rounded up to 16) + 16 * tiles,
+//    where tiles = sum over groups of ceil(M/128) * ceil(N/128). A larger
+//    problem set returns NVFP4_ERR_TOO_LARGE and launches nothing.
+//  * Only NVFP4_SF_PREPACKED scales. The row-major path would need a workspace.
+//  * All calls share the one array. A call overwrites the previous call's table
+//    in stream order. Calls that can overlap on the GPU (on different streams,
+//    without ordering between them) race on it and must not be issued.
+//  * The first call on a device does the set-up: the device checks, the
+//    cudaGetSymbolAddress lookup of the array and the kernel's shared-memory
+//    attribute. Make that first call before any stream capture.
+//  * The error words are cleared at the start of every call. A wait that runs
+//    out inside this kernel ends the launch early, but nvfp4_device_status
+//    does not see it.
+
+namespace {
+
+constexpr size_t kNoAllocScratchBytes = 256 * 1024;
+constexpr size_t kNoAllocStatusBytes = 256;
+
+static __device__ __align__(256) uint8_t g_noalloc_scratch[kNoAllocScratchBytes];
+
+struct NoAllocDevice {
+    bool ready = false;
+    bool supported = false;
+    int sm_count = 0;
+    uint8_t *scratch = nullptr;  // device address of g_noalloc_scratch on this device
+};
+std::mutex g_noalloc_mu;  // guards the per-device set-up and the host staging buffer
+NoAllocDevice g_noalloc_dev[kMaxDevices];
+alignas(128) uint8_t g_noalloc_host[kNoAllocScratchBytes];  // host staging copy of the table
+
+// Once per device, with that device current. The caller holds g_noalloc_mu.
+int noalloc_setup(int dev, NoAllocDevice **out)
+{
+    if (dev < 0 || dev >= kMaxDevices)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    NoAllocDevice &d = g_noalloc_dev[dev];
+    if (!d.ready) {
+        int major = 0, minor = 0, smem = 0;
+        CUDA_TRY(cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
+        CUDA_TRY(cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
+        d.supported = (major == 10 && minor == 3) && smem >= Layout<128, 6>::kSmemBytes;
+        if (d.supported) {
+            void *p = nullptr;
+            CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
+            d.scratch = static_cast<uint8_t *>(p);
+            CUDA_TRY(cudaFuncSetAttribute(nvfp4_grouped_gemm_kernel<128, 6>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<128, 6>::kSmemBytes));
+        }
+        d.ready = true;
+    }
+    if (!d.supported)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    *out = &d;
+    return NVFP4_OK;
+}
+
+}  // namespace
+
+extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp4_stream_t stream_)
+{
+    cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
+    if (g < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (g == 0)
+        return NVFP4_OK;
+    if (!probs)
+        return NVFP4_ERR_INVALID_ARG;
+    for (int i = 0; i < g; ++i) {
+        if (int rc = check_problem(probs[i]))
+            return rc;
+        if (probs[i].sf_layout != NVFP4_SF_PREPACKED)
+            return NVFP4_ERR_INVALID_ARG;
+    }
+
+    // Size the table before touching anything.
+    constexpr int BN = 128;
+    size_t ngroups = 0, ntiles = 0;
+    for (int i = 0; i < g; ++i) {
+        const Nvfp4Problem &p = probs[i];
+        if (p.M == 0 || p.N == 0 || p.K == 0)
+            continue;
+        ++ngroups;
+        ntiles += (size_t)((p.M + kBlockM - 1) / kBlockM) * (size_t)((p.N + BN - 1) / BN);
+    }
+
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    NoAllocDevice *nd = nullptr;
+    if (int rc = noalloc_setup(dev, &nd))
+        return rc;
+    const int cap = g_opt.max_ctas.load() > 0 ? (int)std::min<int64_t>(g_opt.max_ctas.load(), nd->sm_count)
+                                              : nd->sm_count;
+    const int grid = (int)std::max<size_t>(1, std::min<size_t>(ntiles, (size_t)cap));
+    const size_t off_groups = sizeof(TableHeader);
+    const size_t off_cta = off_groups + ngroups * sizeof(GroupEntry);
+    const size_t off_items = (off_cta + (size_t)(grid + 1) * sizeof(uint32_t) + 15) & ~size_t(15);
+    const size_t total = off_items + ntiles * sizeof(WorkItem);
+    if (total > kNoAllocScratchBytes - kNoAllocStatusBytes)
+        return NVFP4_ERR_TOO_LARGE;
+
+    // K == 0: C is the empty sum.
+    for (int i = 0; i < g; ++i) {
+        const Nvfp4Problem &p = probs[i];
+        if (p.M > 0 && p.N > 0 && p.K == 0)
+            CUDA_TRY(cudaMemsetAsync(p.C, 0, (size_t)p.M * p.N * sizeof(__half), stream));
+    }
+    if (ngroups == 0)
+        return NVFP4_OK;
+    if (int rc = get_encoder())
+        return rc;
+
+    // Build the table in the static host buffer, with the same tile order and
+    // CTA assignment as the cached path: group by group, tile_n outer and
+    // tile_m inner, tile t to CTA t % grid.
+    uint8_t *h = g_noalloc_host;
+    memset(h, 0, total);
+    TableHeader *th = reinterpret_cast<TableHeader *>(h);
+    th->num_groups = (int32_t)ngroups;
+    th->num_items = (int32_t)ntiles;
+    th->grid = grid;
+    th->block_n = BN;
+    th->off_cta_begin = (uint32_t)off_cta;
+    th->off_items = (uint32_t)off_items;
+    th->total_bytes = (uint32_t)total;
+    GroupEntry *ge = reinterpret_cast<GroupEntry *>(h + off_groups);
+    uint32_t *cta_begin = reinterpret_cast<uint32_t *>(h + off_cta);
+    WorkItem *items = reinterpret_cast<WorkItem *>(h + off_items);
+    // CTA c holds tiles c, c + grid, c + 2*grid, ...: it gets ceil((ntiles - c) / grid)
+    // of them, and tile t sits at slot cta_begin[t % grid] + t / grid.
+    uint32_t run = 0;
+    for (int c = 0; c < grid; ++c) {
+        cta_begin[c] = run;
+        run += (ntiles > (size_t)c) ? (uint32_t)((ntiles - c + grid - 1) / grid) : 0u;
+    }
+    cta_begin[grid] = run;
+    int gi = 0;
+    size_t t = 0;
+    for (int i = 0; i < g; ++i) {
+        const Nvfp4Problem &p = probs[i];
+        if (p.M == 0 || p.N == 0 || p.K == 0)
+            continue;
+        GroupEntry &e = ge[gi];
+        int rc = encode_operand_map(&e.tmap_a, p.A, (uint64_t)p.K / 2, (uint64_t)p.M, kBlockM);
+        if (!rc)
+            rc = encode_operand_map(&e.tmap_b, p.B, (uint64_t)p.K / 2, (uint64_t)p.N, (uint32_t)BN);
+        if (rc)
+            return rc;
+        e.sfa = static_cast<const uint8_t *>(p.SFA);
+        e.sfb = static_cast<const uint8_t *>(p.SFB);
+        e.C = static_cast<__half *>(p.C);
+        e.M = p.M;
+        e.N = p.N;
+        e.K = p.K;
+        e.kblocks64 = p.K / 64;
+        e.tiles_m = (p.M + kBlockM - 1) / kBlockM;
+        e.tiles_n = (p.N + BN - 1) / BN;
+        for (int n = 0; n < e.tiles_n; ++n)
+            for (int m = 0; m < e.tiles_m; ++m, ++t)
+                items[cta_begin[t % grid] + t / grid] = WorkItem{gi, m, n, 0};
+        ++gi;
+    }
+
+    uint8_t *dscratch = nd->scratch;
+    int *dstatus = reinterpret_cast<int *>(dscratch);
+    const Table *dtable = reinterpret_cast<const Table *>(dscratch + kNoAllocStatusBytes);
+    CUDA_TRY(cudaMemsetAsync(dstatus, 0, kNoAllocStatusBytes, stream));
+    // From pageable memory: returns once the bytes are staged, so the host
+    // buffer may be reused by the next call.
+    CUDA_TRY(cudaMemcpyAsync(dscratch + kNoAllocStatusBytes, h, total, cudaMemcpyHostToDevice, stream));
+
+    KernelArgs args{};
+    args.table = dtable;
+    args.status = dstatus;
+    args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
+    args.fault_skip_load = -1;
+    args.num_groups = (int32_t)ngroups;
+    nvfp4_grouped_gemm_kernel<128, 6><<<grid, kThreads, Layout<128, 6>::kSmemBytes, stream>>>(args);
+    CUDA_TRY(cudaGetLastError());
+    return NVFP4_OK;
+}

@@ -157,6 +157,41 @@ int nvfp4_set_option(int option, int64_t value);
  * device that holds one. Calls made afterwards start again from empty caches. */
 void nvfp4_release(void);
 
+/* The grouped GEMM for callers that cannot allocate device memory. The pages
+ * have no counterpart: this is a library convenience.
+ *
+ * Who needs it: code that must not call cudaMalloc/cudaFree, or anything that
+ * allocates on the device. Examples: code running inside a custom device
+ * allocator or an out-of-memory handler, or a runtime that owns every byte of
+ * device memory and forbids libraries to take more. nvfp4_grouped_gemm
+ * allocates its cached problem tables, its error word and (for row-major
+ * scales) a workspace. This entry point allocates none of them. Its only
+ * device memory beyond the caller's A, B, SFA, SFB and C is one fixed 256 KB
+ * array built into the library. Every GPU that loads the library holds that
+ * array until the process exits.
+ *
+ * Same arguments and results as nvfp4_grouped_gemm, with these limits:
+ *  - Scales must be NVFP4_SF_PREPACKED. Otherwise NVFP4_ERR_INVALID_ARG.
+ *  - The problem table must fit the array:
+ *      128 + 384*g' + 4*(grid+1) (rounded up to 16) + 16*tiles <= 262144 - 256 bytes,
+ *    where g' counts the groups with M, N, K > 0,
+ *    tiles = sum ceil(M/128)*ceil(N/128) and grid = min(tiles, SM count).
+ *    In practice that is up to about 16,000 tiles of 128 x 128 for a few
+ *    groups. A larger set returns NVFP4_ERR_TOO_LARGE and launches nothing.
+ *  - Every call shares the one array. A call rewrites the table in stream
+ *    order, and a kernel that is still running on another stream would read
+ *    the new table: calls that can overlap on the GPU race and must not be made.
+ *  - The first call on each device does a one-time set-up with that device
+ *    current: it checks the device, looks up the array's device address
+ *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit. Make that
+ *    first call before any stream capture.
+ *  - The kernel's error words live in the same array. They are cleared at the
+ *    start of each call and nvfp4_device_status() does not read them, so a
+ *    wait that runs out in this kernel is not reported.
+ * Each call encodes its tensor maps and copies the table (a few KB) from a
+ * static host buffer before the launch. There is no cache. */
+int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp4_stream_t stream);
+
 #ifdef __cplusplus
 }
 #endif
