@@ -120,8 +120,8 @@ int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, void *sf_bloc
  *  *status = NVFP4_OK, or NVFP4_ERR_TIMEOUT if any launch since the last read
  *  gave up a wait.
  *  detail (may be NULL) receives 4 words: the code, the role (0 producer,
- *  1 MMA, 2 epilogue, 3 teardown), the work item and the k-stage at which the
- *  first timeout happened.
+ *  1 MMA issuer, 2 epilogue, 3 teardown, 4 scale stagers), the work item and
+ *  the k-stage at which the first timeout happened.
  * Returns NVFP4_OK or an NVFP4_ERR_* code of its own. */
 int nvfp4_device_status(nvfp4_stream_t stream, int *status, int32_t *detail);
 
