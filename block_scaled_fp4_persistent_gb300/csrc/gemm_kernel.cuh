@@ -1,37 +1,44 @@
 // gemm_kernel.cuh -- the persistent, warp-specialised grouped NVFP4 GEMM kernel.
 //
-// One CTA per SM walks its own list of output tiles (group, 128-row tile m,
-// BLOCK_N-column tile n). Ten warps share the work:
+// One CTA per SM (a kernel that allocates TMEM gets no second CTA on an SM).
+// Each CTA walks its own list of output tiles of 128 rows x BN columns
+// (group, tile m, tile n). Fourteen warps share the work:
 //   warp 0      TMA producer. It streams 256-wide K-stages of A and B (E2M1,
 //               128-byte swizzled rows) and the matching 512-byte scale blocks
 //               into a ring of STAGES shared-memory slots.
-//   warp 1      MMA issuer; it also owns the TMEM allocation. Per stage it issues
-//               four block-scaled MMAs (kind::mxf4nvf4, 16-element scale blocks,
-//               K = 64 each) into one of two TMEM accumulators, then commits the
-//               stage back to the producer.
-//   warps 2-5   epilogue. They load the fp32 accumulator from TMEM, free it for
-//               the next tile, round to fp16 and store the rows that lie inside
-//               the group.
-//   warps 6-9   scale stagers. Per stage each warp reads its rows of the scale
+//   warp 1      MMA issuer; it also owns the TMEM allocation. Per stage it
+//               issues four block-scaled MMAs (kind::mxf4nvf4, 16-element scale
+//               blocks, M = 128, N = BN, K = 64 each) into the TMEM accumulator,
+//               then commits the stage back to the producer.
+//   warps 2-5   scale stagers. Per stage each warp reads its rows of the scale
 //               blocks from shared memory and writes them into the stage's TMEM
-//               scale slot with tcgen05.st, in the layout tcgen05.cp .warpx4
-//               would produce.
-// The two accumulators let tile t+1's MMAs run while tile t is stored.
+//               scale slot with tcgen05.st, in the layout that
+//               tcgen05.cp .32x128b.warpx4 would produce.
+//   warps 6-13  epilogue. Two warps per TMEM lane quarter, each owning BN/2
+//               columns. They drain the accumulator to registers (converting to
+//               fp16 on the way), free it for the next tile's MMAs, then store the
+//               rows that lie inside the group.
 //
-// Why the stagers exist. On this GPU one tcgen05.cp of a 512-byte scale block
-// costs about as much tensor-pipe time as an MMA (measured: ~46 vs ~64 cycles),
-// and a 256-wide stage needs 8 of them for 4 MMAs. Issued from the MMA thread,
-// the copies more than double the per-stage pipe time. tcgen05.st from four
-// other warps writes the same TMEM contents while the MMAs run.
+// Why this shape. Measurements on this GPU drove it:
+//  * One tcgen05.cp of a 512-byte scale block costs about as much tensor-pipe
+//    time as an N = 128 MMA (~46 vs ~64 cycles), and a stage needs 8 or 12.
+//    So the scales are written with tcgen05.st by other warps while MMAs run.
+//  * The issuing thread pays ~100 cycles per tcgen05 instruction and ~300 per
+//    stage for its barrier wait and commit, whatever the MMA's N. N = 256 MMAs
+//    (BN = 256) halve the issue cost per output and the A re-reads per output.
+//  * With BN = 256 the accumulator takes half of TMEM. It is single-buffered:
+//    eight epilogue warps drain it in a few hundred cycles, and the next tile's
+//    MMAs start while those warps store the previous tile.
 //
 // The pages' kernels (page 1 `grouped_gemm_kernel_v4`, page 2
-// `group_gemm_kernel_impl`) use the producer/MMA/epilogue split and copy the
-// scales with tcgen05.cp from the MMA thread. This kernel differs from them in
-// several ways. Scale staging is moved off the MMA thread. Ring and accumulator
-// phases are monotone counters carried across tiles, so no barrier is
-// re-initialised. The schedule is a per-CTA list built on the host. There is no
-// cluster multicast. Every wait is bounded: when one runs out, the kernel
-// records an error word and returns, and it never traps.
+// `group_gemm_kernel_impl`) copy the scales with tcgen05.cp from the MMA thread,
+// and page 1 also runs 128 x 256 tiles for N >= 4096. Other differences:
+//  * ring phases are monotone counters carried across tiles, so no barrier is
+//    re-initialised;
+//  * the schedule is a per-CTA list built on the host;
+//  * there is no cluster multicast;
+//  * every wait is bounded. When one runs out, the kernel records an error
+//    word and returns, and it never traps.
 #pragma once
 #include <cuda_fp16.h>
 #include <cstdint>
@@ -41,15 +48,16 @@
 
 namespace nvfp4 {
 
-constexpr int kThreads = 320;
+constexpr int kPipes = 1;                // tile lists per CTA
 constexpr int kProducerWarp = 0;
 constexpr int kMmaWarp = 1;
-constexpr int kEpilogueWarp0 = 2;  // warps 2..5
-constexpr int kScaleWarp0 = 6;     // warps 6..9
+constexpr int kStagerWarp0 = 2;          // warps 2..5
+constexpr int kEpilogueWarp0 = 6;        // warps 6..13
+constexpr int kEpilogueWarps = 8;
+constexpr int kThreads = (kEpilogueWarp0 + kEpilogueWarps) * 32;
 constexpr int kBlockM = 128;
 constexpr int kBlockK = 256;             // K per stage = 128 bytes of E2M1 per row
 constexpr int kRowBytes = kBlockK / 2;   // 128
-constexpr int kMmaK = 64;                // K per MMA
 constexpr int kScaleBlockBytes = 512;    // scales of 128 rows x 64 K
 constexpr uint32_t kTmemCols = 512;
 
@@ -58,24 +66,27 @@ constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleTeardown 
 
 template <int BN, int STAGES>
 struct Layout {
+    static constexpr int kHalves = BN / 128;                       // 128-row halves of the B tile
     static constexpr int kABytes = kBlockM * kRowBytes;            // 16 KB
-    static constexpr int kBBytes = BN * kRowBytes;                 // 16 KB for BN = 128
+    static constexpr int kBBytes = BN * kRowBytes;                 // 32 KB for BN = 256
     static constexpr int kSfaBytes = 4 * kScaleBlockBytes;         // 2 KB
-    static constexpr int kSfbBytes = (BN / 128) * 4 * kScaleBlockBytes;
+    static constexpr int kSfbBytes = kHalves * 4 * kScaleBlockBytes;
     static constexpr int kStageBytes = kABytes + kBBytes + kSfaBytes + kSfbBytes;
     static constexpr int kOffB = kABytes;
     static constexpr int kOffSfa = kABytes + kBBytes;
-    static constexpr int kOffSfb = kOffSfa + kSfaBytes;
+    static constexpr int kOffSfb = kOffSfa + kSfaBytes;            // half h, k-block j at + (4h + j) * 512
     static constexpr int kRingBytes = STAGES * kStageBytes;
-    // barriers: full[S], empty[S], sf_full[S], acc_full[2], acc_empty[2], drain, then the TMEM base word
-    static constexpr int kBarBytes = (3 * STAGES + 5) * 8 + 16;
+    // barriers: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain, then the TMEM base word
+    static constexpr int kBarBytes = (3 * STAGES + 3) * 8 + 16;
     static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + 64;
-    // TMEM columns: accumulators at 0 and BN; a 32-column scale slot per stage after them
-    // (SFA at +0..15: k-block j at +4j; SFB at +16..31)
-    static constexpr uint32_t kSfCol0 = 2 * BN;
-    static constexpr uint32_t kSfColsPerStage = 32;
+    // TMEM columns: the accumulator at 0 .. BN-1, then one scale slot per stage:
+    //   SFA at +0 .. 15 (k-block j at +4j),
+    //   SFB at +16 .. (k-block j at +16 + 4*kHalves*j; its half h at +4h within that).
+    static constexpr uint32_t kSfbCol = 16;
+    static constexpr uint32_t kSfColsPerStage = 16 + 16 * kHalves;
+    static constexpr uint32_t kSfCol0 = BN;
     static_assert(kStageBytes % 1024 == 0, "stage slots must keep 1024-byte alignment");
-    static_assert(2 * BN + STAGES * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
+    static_assert(BN + STAGES * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
 };
 
 struct SharedState {
@@ -118,7 +129,7 @@ __device__ __forceinline__ bool wait_phase(uint32_t bar, uint32_t parity, Shared
 
 // The same wait for a whole warp: lane 0 polls, the verdict is shared, and
 // every lane then takes its own acquire of the completed phase (which cannot
-// move on before this warp releases the slot).
+// move on before this warp releases it).
 __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, SharedState *sh,
                                                 const KernelArgs &args, int role, int item, int stage)
 {
@@ -131,10 +142,28 @@ __device__ __forceinline__ bool warp_wait_phase(uint32_t bar, uint32_t parity, S
     return ok != 0;
 }
 
+// Bounded wait that ignores the abort flag, for the teardown drains.
+__device__ __forceinline__ void drain_wait(uint32_t bar, uint32_t parity, const KernelArgs &args, int stage)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity)) {
+        if (global_timer_ns() - t0 > args.timeout_ns) {
+            record_error(args.status, kStatusTimeout, kRoleTeardown, -1, stage);
+            return;
+        }
+    }
+}
+
+__device__ __forceinline__ uint32_t pack_half2(uint32_t lo, uint32_t hi)
+{
+    __half2 h = __floats2half2_rn(__uint_as_float(lo), __uint_as_float(hi));
+    return *reinterpret_cast<uint32_t *>(&h);
+}
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const __grid_constant__ KernelArgs args)
 {
-    static_assert(BN == 128, "only 128-column tiles: the TMEM scale layout of N = 256 is not used");
+    static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     using L = Layout<BN, STAGES>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // 1024-byte alignment for the 128-byte swizzle pattern of the operand tiles
@@ -145,8 +174,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     uint64_t *empty = bars + STAGES;
     uint64_t *sf_full = bars + 2 * STAGES;
     uint64_t *acc_full = bars + 3 * STAGES;
-    uint64_t *acc_empty = acc_full + 2;
-    uint64_t *drain = acc_empty + 2;
+    uint64_t *acc_empty = acc_full + 1;
+    uint64_t *drain = acc_empty + 1;
     uint32_t *tmem_base_word = reinterpret_cast<uint32_t *>(drain + 1);
     SharedState *sh = reinterpret_cast<SharedState *>(tmem_base_word + 2);
 
@@ -162,10 +191,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             mbar_init(smem_addr(&empty[s]), 1);
             mbar_init(smem_addr(&sf_full[s]), 4);  // one elected arrive per stager warp
         }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(smem_addr(&acc_full[b]), 1);
-            mbar_init(smem_addr(&acc_empty[b]), 4 * 32);
-        }
+        mbar_init(smem_addr(acc_full), 1);
+        mbar_init(smem_addr(acc_empty), kEpilogueWarps);  // one elected arrive per epilogue warp
         mbar_init(smem_addr(drain), 1);
         sh->abort = 0;
         fence_barrier_init();
@@ -178,9 +205,14 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *tmem_base_word;
+    const uint32_t tmem_sf = tmem_base + L::kSfCol0;
 
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
+        // Besides the ring's loads, the producer keeps an L2 prefetch cursor
+        // args.prefetch_stages stages ahead of them, across tile boundaries: the
+        // ring holds only STAGES stages, and a stage that comes from DRAM takes
+        // ~1.5 us to land, while one that comes from L2 lands several times sooner.
         if (lane == 0) {
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b_stream = policy_evict_first();
@@ -189,38 +221,87 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 tensormap_prefetch(&tab->group(gi).tmap_a);
                 tensormap_prefetch(&tab->group(gi).tmap_b);
             }
+            struct Src {  // where one tile's stages come from
+                const void *tmap_a, *tmap_b;
+                int32_t ya, yb;
+                int kb64, nk;
+                bool b_shared;
+                const uint8_t *sfa;
+                const uint8_t *sfb[L::kHalves];
+            };
+            auto source = [&](uint32_t it) {
+                Src r;
+                const WorkItem w = tab->item(it);
+                const GroupEntry &ge = tab->group(w.group);
+                r.tmap_a = &ge.tmap_a;
+                r.tmap_b = &ge.tmap_b;
+                r.ya = w.tile_m * kBlockM;
+                r.yb = w.tile_n * BN;
+                r.kb64 = ge.kblocks64;
+                r.nk = (r.kb64 + 3) / 4;
+                r.b_shared = ge.tiles_m > 1;
+                r.sfa = ge.sfa + (size_t)w.tile_m * r.kb64 * kScaleBlockBytes;
+                // The scales of B come in 128-row tiles. A half of the B tile that lies
+                // wholly past N reads the first half's scales instead: its B rows are
+                // zero (TMA fills them), so the scales only need to be finite.
+                const int rt_b = (ge.N + 127) / 128;
+#pragma unroll
+                for (int h = 0; h < L::kHalves; ++h) {
+                    const int rt = w.tile_n * L::kHalves + h;
+                    r.sfb[h] = ge.sfb + (size_t)(rt < rt_b ? rt : w.tile_n * L::kHalves) * r.kb64 * kScaleBlockBytes;
+                }
+                return r;
+            };
+            // prefetch cursor
+            uint32_t pf_it = item_begin, pf_g = 0;
+            int pf_kb = 0;
+            Src pf{};
+            if (pf_it < item_end)
+                pf = source(pf_it);
+            auto prefetch_until = [&](uint32_t g_end) {
+                while (pf_g < g_end && pf_it < item_end) {
+                    const uint32_t sfb_bytes = (uint32_t)min(4, pf.kb64 - pf_kb * 4) * kScaleBlockBytes;
+                    tma_prefetch_2d(pf.tmap_a, pf_kb * kRowBytes, pf.ya);
+                    tma_prefetch_2d(pf.tmap_b, pf_kb * kRowBytes, pf.yb);
+                    bulk_prefetch(pf.sfa + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
+#pragma unroll
+                    for (int h = 0; h < L::kHalves; ++h)
+                        bulk_prefetch(pf.sfb[h] + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
+                    ++pf_g;
+                    if (++pf_kb == pf.nk) {
+                        pf_kb = 0;
+                        if (++pf_it < item_end)
+                            pf = source(pf_it);
+                    }
+                }
+            };
+            const uint32_t pf_dist = (uint32_t)args.prefetch_stages;
             uint32_t stage = 0, phase = 0, kiter = 0;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-                const WorkItem w = tab->item(it);
-                const GroupEntry &ge = tab->group(w.group);
-                const int kb64 = ge.kblocks64;
-                const int nk = (kb64 + 3) / 4;
-                const uint64_t pol_b = ge.tiles_m > 1 ? pol_b_shared : pol_b_stream;
-                const void *tmap_a = &ge.tmap_a;
-                const void *tmap_b = &ge.tmap_b;
-                const int32_t ya = w.tile_m * kBlockM, yb = w.tile_n * BN;
-                const uint8_t *sfa = ge.sfa + (size_t)w.tile_m * kb64 * kScaleBlockBytes;
-                const uint8_t *sfb = ge.sfb + (size_t)w.tile_n * (BN / 128) * kb64 * kScaleBlockBytes;
-                for (int kb = 0; kb < nk; ++kb, ++kiter) {
+                const Src src = source(it);
+                const uint64_t pol_b = src.b_shared ? pol_b_shared : pol_b_stream;
+                for (int kb = 0; kb < src.nk; ++kb, ++kiter) {
+                    if (pf_dist > 0)
+                        prefetch_until(kiter + pf_dist);
                     if (!wait_phase(smem_addr(&empty[stage]), phase ^ 1u, sh, args, kRoleProducer, (int)it, kb)) {
                         ok = false;
                         break;
                     }
-                    const int ksub = min(4, kb64 - kb * 4);
+                    const int ksub = min(4, src.kb64 - kb * 4);
                     const uint32_t sf_bytes = (uint32_t)ksub * kScaleBlockBytes;
-                    const uint32_t bytes = L::kABytes + L::kBBytes + sf_bytes * (1 + BN / 128);
+                    const uint32_t bytes = L::kABytes + L::kBBytes + sf_bytes * (1 + L::kHalves);
                     const uint32_t slot = smem_addr(ring + stage * L::kStageBytes);
                     const uint32_t fb = smem_addr(&full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!(args.fault_skip_load >= 0 && blockIdx.x == 0 && kiter == (uint32_t)args.fault_skip_load)) {
-                        tma_load_2d(slot, tmap_a, kb * kRowBytes, ya, fb, pol_a);
-                        tma_load_2d(slot + L::kOffB, tmap_b, kb * kRowBytes, yb, fb, pol_b);
-                        bulk_load(slot + L::kOffSfa, sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
+                        tma_load_2d(slot, src.tmap_a, kb * kRowBytes, src.ya, fb, pol_a);
+                        tma_load_2d(slot + L::kOffB, src.tmap_b, kb * kRowBytes, src.yb, fb, pol_b);
+                        bulk_load(slot + L::kOffSfa, src.sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
 #pragma unroll
-                        for (int h = 0; h < BN / 128; ++h)
+                        for (int h = 0; h < L::kHalves; ++h)
                             bulk_load(slot + L::kOffSfb + h * 4 * kScaleBlockBytes,
-                                      sfb + ((size_t)h * kb64 + kb * 4) * kScaleBlockBytes, sf_bytes, fb, pol_b);
+                                      src.sfb[h] + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_b);
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -234,141 +315,85 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             const uint32_t issued = kiter < (uint32_t)STAGES ? kiter : (uint32_t)STAGES;
             for (uint32_t i = 0; i < issued; ++i) {
                 const uint32_t f = kiter - 1 - i;
-                const uint32_t s = f % STAGES, ph = (f / STAGES) & 1u;
-                uint64_t t0 = global_timer_ns();
-                while (!mbar_try_wait(smem_addr(&full[s]), ph)) {
-                    if (global_timer_ns() - t0 > args.timeout_ns) {
-                        record_error(args.status, kStatusTimeout, kRoleTeardown, -1, (int)s);
-                        break;
-                    }
-                }
+                drain_wait(smem_addr(&full[f % STAGES]), (f / STAGES) & 1u, args, (int)(f % STAGES));
             }
         }
     } else if (warp == kMmaWarp) {
         // ------------------------------------------------------ MMA issuer
+        // This thread is on the critical path, so its loop is short: descriptors
+        // and TMEM addresses advance by constant steps and are never rebuilt.
         if (lane == 0) {
             constexpr uint32_t idesc = mma_idesc_nvfp4(kBlockM, BN);
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            constexpr uint64_t kDescStep = (uint64_t)(L::kStageBytes >> 4);  // one ring slot, in 16-byte units
+            constexpr uint32_t kB = L::kSfbCol, kJ = 4 * L::kHalves;          // SFB column of k-block j: kB + kJ*j
+            const uint64_t desc_a0 = operand_desc(smem_addr(ring));
+            const uint64_t desc_b0 = operand_desc(smem_addr(ring) + L::kOffB);
+            uint32_t stage = 0, phase = 0, acc_phase = 0;
+            uint64_t da = desc_a0, db = desc_b0;
+            uint32_t sf = tmem_sf;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = tab->item(it);
                 const int kb64 = tab->group(w.group).kblocks64;
                 const int nk = (kb64 + 3) / 4;
-                if (!wait_phase(smem_addr(&acc_empty[acc]), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
+                // the epilogue warps must have drained the previous tile's accumulator
+                if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
                     ok = false;
                     break;
                 }
+                acc_phase ^= 1u;
                 tc_fence_after();
-                const uint32_t d_tmem = tmem_base + acc * BN;
                 for (int kb = 0; kb < nk; ++kb) {
-                    // The stagers arrive on sf_full only after the stage's copies landed, so
-                    // the full wait below returns at once; it gives this thread its own
-                    // acquire of the TMA writes that the MMAs read.
-                    if (!wait_phase(smem_addr(&sf_full[stage]), phase, sh, args, kRoleMma, (int)it, kb) ||
-                        !wait_phase(smem_addr(&full[stage]), phase, sh, args, kRoleMma, (int)it, kb)) {
+                    // sf_full is released by the stagers only after they acquired the
+                    // stage's full barrier, so the TMA writes of A and B are ordered
+                    // before this wait.
+                    if (!wait_phase(smem_addr(&sf_full[stage]), phase, sh, args, kRoleMma, (int)it, kb)) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const int ksub = min(4, kb64 - kb * 4);
-                    const uint32_t slot = smem_addr(ring + stage * L::kStageBytes);
-                    const uint32_t sfa_col = tmem_base + L::kSfCol0 + stage * L::kSfColsPerStage;
-                    const uint32_t sfb_col = sfa_col + 16;
-                    const uint32_t acc_in = kb > 0 ? 1u : 0u;
-                    if (ksub == 4) {
-#pragma unroll
-                        for (int j = 0; j < 4; ++j)
-                            tc_mma_nvfp4(d_tmem, operand_desc(slot + j * 32), operand_desc(slot + L::kOffB + j * 32),
-                                         idesc, sfa_col + 4 * j, sfb_col + 4 * j, (acc_in | (uint32_t)j) ? 1u : 0u);
+                    const uint32_t acc0 = kb > 0 ? 1u : 0u;
+                    if (kb64 - kb * 4 >= 4) {
+                        // K step of 64 E2M1 = 32 bytes inside the 128-byte swizzled row: +2 in the
+                        // descriptor's 16-byte address field
+                        tc_mma_nvfp4(tmem_base, da + 0, db + 0, idesc, sf + 0, sf + kB, acc0);
+                        tc_mma_nvfp4(tmem_base, da + 2, db + 2, idesc, sf + 4, sf + kB + kJ, 1u);
+                        tc_mma_nvfp4(tmem_base, da + 4, db + 4, idesc, sf + 8, sf + kB + 2 * kJ, 1u);
+                        tc_mma_nvfp4(tmem_base, da + 6, db + 6, idesc, sf + 12, sf + kB + 3 * kJ, 1u);
                     } else {
+                        const int ksub = kb64 - kb * 4;
                         for (int j = 0; j < ksub; ++j)
-                            tc_mma_nvfp4(d_tmem, operand_desc(slot + j * 32), operand_desc(slot + L::kOffB + j * 32),
-                                         idesc, sfa_col + 4 * j, sfb_col + 4 * j, (acc_in | (uint32_t)j) ? 1u : 0u);
+                            tc_mma_nvfp4(tmem_base, da + 2 * j, db + 2 * j, idesc, sf + 4 * j, sf + kB + kJ * j,
+                                         (acc0 | (uint32_t)j) ? 1u : 0u);
                     }
                     tc_commit(smem_addr(&empty[stage]));
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
+                        da = desc_a0;
+                        db = desc_b0;
+                        sf = tmem_sf;
+                    } else {
+                        da += kDescStep;
+                        db += kDescStep;
+                        sf += L::kSfColsPerStage;
                     }
                 }
                 if (!ok)
                     break;
-                tc_commit(smem_addr(&acc_full[acc]));
-                if (++acc == 2) {
-                    acc = 0;
-                    acc_phase ^= 1u;
-                }
+                tc_commit(smem_addr(acc_full));
             }
             // Every MMA this thread issued must finish before TMEM is freed.
             tc_commit(smem_addr(drain));
-            uint64_t t0 = global_timer_ns();
-            while (!mbar_try_wait(smem_addr(drain), 0)) {
-                if (global_timer_ns() - t0 > args.timeout_ns) {
-                    record_error(args.status, kStatusTimeout, kRoleTeardown, -1, -1);
-                    break;
-                }
-            }
+            drain_wait(smem_addr(drain), 0, args, -1);
         }
-    } else if (warp < kScaleWarp0) {
-        // ------------------------------------------------------ epilogue
-        const int quarter = warp % 4;  // warps 2,3,4,5 -> TMEM lane quarters 2,3,0,1
-        const int row_in_tile = quarter * 32 + (int)lane;
-        uint32_t acc = 0, acc_phase = 0;
-        for (uint32_t it = item_begin; it < item_end; ++it) {
-            const WorkItem w = tab->item(it);
-            const GroupEntry &ge = tab->group(w.group);
-            const int M = ge.M, N = ge.N;
-            __half *const C = ge.C;
-            if (!wait_phase(smem_addr(&acc_full[acc]), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
-                break;
-            tc_fence_after();
-            const uint32_t t_addr = tmem_base + ((uint32_t)(quarter * 32) << 16) + acc * BN;
-            uint32_t v[BN / 32][32];
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-                tmem_load_32cols(t_addr + c * 32, v[c]);
-            tmem_load_wait();
-#pragma unroll
-            for (int c = 0; c < BN / 32; ++c)
-                reg_fence(v[c]);
-            tc_fence_before();
-            mbar_arrive(smem_addr(&acc_empty[acc]));
-            if (++acc == 2) {
-                acc = 0;
-                acc_phase ^= 1u;
-            }
-            const int m = w.tile_m * kBlockM + row_in_tile;
-            if (m < M) {
-                const int n0 = w.tile_n * BN;
-                __half *crow = C + (size_t)m * N + n0;
-#pragma unroll
-                for (int c = 0; c < BN / 32; ++c) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int col = c * 32 + q * 8;
-                        if (n0 + col < N) {
-                            uint4 pk;
-                            __half2 h0 = __floats2half2_rn(__uint_as_float(v[c][q * 8 + 0]), __uint_as_float(v[c][q * 8 + 1]));
-                            __half2 h1 = __floats2half2_rn(__uint_as_float(v[c][q * 8 + 2]), __uint_as_float(v[c][q * 8 + 3]));
-                            __half2 h2 = __floats2half2_rn(__uint_as_float(v[c][q * 8 + 4]), __uint_as_float(v[c][q * 8 + 5]));
-                            __half2 h3 = __floats2half2_rn(__uint_as_float(v[c][q * 8 + 6]), __uint_as_float(v[c][q * 8 + 7]));
-                            pk.x = *reinterpret_cast<uint32_t *>(&h0);
-                            pk.y = *reinterpret_cast<uint32_t *>(&h1);
-                            pk.z = *reinterpret_cast<uint32_t *>(&h2);
-                            pk.w = *reinterpret_cast<uint32_t *>(&h3);
-                            *reinterpret_cast<uint4 *>(crow + col) = pk;
-                        }
-                    }
-                }
-            }
-        }
-    } else {
+    } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------ scale stagers
         // Lane r of the warp for TMEM lane quarter q writes TMEM lane 32q + r. Word c of
-        // k-block j goes to column 4j + c: the scales of row r + 32c, i.e. bytes
-        // 4c..4c+3 of row r of the block. That is the layout tcgen05.cp .32x128b.warpx4
+        // a 512-byte block's row r holds the 4 k-scales of row r + 32c; it goes to the
+        // block's column base + c. That is the layout tcgen05.cp .32x128b.warpx4
         // produces, repeated in all four quarters.
-        const int quarter = warp % 4;  // warps 6,7,8,9 -> quarters 2,3,0,1
+        const int quarter = warp % 4;  // warps 2,3,4,5 -> quarters 2,3,0,1
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t stage = 0, phase = 0;
         bool ok = true;
@@ -382,17 +407,28 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     break;
                 }
                 const uint8_t *src = ring + stage * L::kStageBytes + L::kOffSfa + lane * 16;
-                uint32_t ra[16], rb[16];
+                const uint32_t col = tmem_sf + lane_off + stage * L::kSfColsPerStage;
+                uint32_t ra[16];
 #pragma unroll
                 for (int j = 0; j < 4; ++j) {
                     const uint4 a = *reinterpret_cast<const uint4 *>(src + j * kScaleBlockBytes);
-                    const uint4 b = *reinterpret_cast<const uint4 *>(src + L::kSfaBytes + j * kScaleBlockBytes);
                     ra[4 * j + 0] = a.x, ra[4 * j + 1] = a.y, ra[4 * j + 2] = a.z, ra[4 * j + 3] = a.w;
-                    rb[4 * j + 0] = b.x, rb[4 * j + 1] = b.y, rb[4 * j + 2] = b.z, rb[4 * j + 3] = b.w;
                 }
-                const uint32_t col = tmem_base + lane_off + L::kSfCol0 + stage * L::kSfColsPerStage;
                 tmem_store_16cols(col, ra);
-                tmem_store_16cols(col + 16, rb);
+                // SFB: columns in order (k-block j, half h, word c), 16 per store
+#pragma unroll
+                for (int batch = 0; batch < L::kHalves; ++batch) {
+                    uint32_t rb[16];
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int idx = batch * 4 + x;  // 0 .. 4*kHalves-1: the (j, h) block in column order
+                        const int j = idx / L::kHalves, h = idx % L::kHalves;
+                        const uint4 b = *reinterpret_cast<const uint4 *>(src + L::kSfaBytes +
+                                                                         (h * 4 + j) * kScaleBlockBytes);
+                        rb[4 * x + 0] = b.x, rb[4 * x + 1] = b.y, rb[4 * x + 2] = b.z, rb[4 * x + 3] = b.w;
+                    }
+                    tmem_store_16cols(col + L::kSfbCol + 16 * batch, rb);
+                }
                 tmem_store_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -401,6 +437,54 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
+                }
+            }
+        }
+    } else {
+        // ------------------------------------------------------ epilogue
+        // Warp w owns TMEM lane quarter w % 4 and the column half (w - 6) / 4 of the
+        // accumulator: output row tile_m*128 + 32*(w % 4) + lane, columns
+        // half*BN/2 .. half*BN/2 + BN/2 - 1 of the tile.
+        const int quarter = warp % 4;  // warps 6..13 -> quarters 2,3,0,1,2,3,0,1
+        const int chalf = (warp - kEpilogueWarp0) / 4;
+        constexpr int kCols = BN / 2;
+        const uint32_t t_addr = tmem_base + ((uint32_t)(quarter * 32) << 16) + chalf * kCols;
+        const int row_in_tile = quarter * 32 + (int)lane;
+        uint32_t acc_phase = 0;
+        for (uint32_t it = item_begin; it < item_end; ++it) {
+            const WorkItem w = tab->item(it);
+            const GroupEntry &ge = tab->group(w.group);
+            const int M = ge.M, N = ge.N;
+            __half *const C = ge.C;
+            if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
+                break;
+            acc_phase ^= 1u;
+            tc_fence_after();
+            // drain: 32 columns at a time, packed to fp16 pairs as they arrive
+            uint32_t hv[kCols / 2];
+#pragma unroll
+            for (int c = 0; c < kCols / 32; ++c) {
+                uint32_t v[32];
+                tmem_load_32cols(t_addr + c * 32, v);
+                tmem_load_wait();
+                reg_fence(v);
+#pragma unroll
+                for (int i = 0; i < 16; ++i)
+                    hv[c * 16 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0)
+                mbar_arrive(smem_addr(acc_empty));
+            const int m = w.tile_m * kBlockM + row_in_tile;
+            const int n0 = w.tile_n * BN + chalf * kCols;
+            if (m < M) {
+                __half *crow = C + (size_t)m * N + n0;
+#pragma unroll
+                for (int q = 0; q < kCols / 8; ++q) {
+                    if (n0 + q * 8 < N)
+                        *reinterpret_cast<uint4 *>(crow + q * 8) =
+                            make_uint4(hv[4 * q + 0], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
                 }
             }
         }

@@ -45,9 +45,18 @@ struct Options {
     std::atomic<int64_t> max_ctas{0};
     std::atomic<int64_t> timeout_us{2000000};
     std::atomic<int64_t> fault_skip_load{-1};
+    std::atomic<int64_t> prefetch_stages{-1};  // -1 = automatic
 } g_opt;
 
 constexpr int kMaxDevices = 64;
+// Kernel variants: BLOCK_N 128 or 256, each with the deepest ring that fits in
+// shared memory, or a 2-stage ring (for tests).
+constexpr int kDefaultBlockN = 128;
+constexpr int kDeepStages128 = 6;  // 6 x 36 KB
+constexpr int kDeepStages256 = 4;  // 4 x 54 KB
+constexpr int kDefaultStages = kDefaultBlockN == 256 ? kDeepStages256 : kDeepStages128;
+// How far ahead of the ring the producer prefetches into L2, in stages.
+constexpr int kDefaultPrefetchStages = 0;
 constexpr int kMaxDim = 1 << 24;
 constexpr size_t kMaxCachedTables = 32;
 
@@ -196,12 +205,17 @@ struct ActiveGroup {
     void *C;
 };
 
-// Per-CTA tile lists. Tiles are numbered group by group, and inside a group
-// B-strip by B-strip (tile_n outer, tile_m inner). Tile t goes to CTA t % grid.
-// So the CTAs that run at the same moment hold consecutive tiles: the m-tiles
-// that share one strip of B read it from HBM once and from L2 after that.
+// Tile lists. The kernel runs kPipes pipelines per CTA, and each pipeline walks
+// its own list; list number c * kPipes + p belongs to pipeline p of CTA c.
+// Tiles are numbered group by group, and inside a group B-strip by B-strip
+// (tile_n outer, tile_m inner). Tile t goes to CTA t % grid, pipeline
+// (t / grid) % kPipes. So the CTAs that run at the same moment hold
+// consecutive tiles: the m-tiles that share one strip of B read it from HBM
+// once and from L2 after that. Each SM's two pipelines take alternate waves.
+inline int list_of_tile(size_t t, int grid) { return (int)(t % grid) * kPipes + (int)((t / grid) % kPipes); }
+
 void build_schedule(const std::vector<ActiveGroup> &gs, int block_n, int grid_cap, std::vector<WorkItem> &items,
-                    std::vector<uint32_t> &cta_begin, int &grid)
+                    std::vector<uint32_t> &list_begin, int &grid)
 {
     std::vector<WorkItem> order;
     for (int gi = 0; gi < (int)gs.size(); ++gi) {
@@ -211,22 +225,25 @@ void build_schedule(const std::vector<ActiveGroup> &gs, int block_n, int grid_ca
                 order.push_back(WorkItem{gi, m, n, 0});
     }
     grid = std::max(1, std::min<int>((int)order.size(), grid_cap));
+    const int lists = grid * kPipes;
+    std::vector<std::vector<WorkItem>> per(lists);
+    for (size_t t = 0; t < order.size(); ++t)
+        per[list_of_tile(t, grid)].push_back(order[t]);
     items.clear();
-    cta_begin.assign(grid + 1, 0);
-    for (int c = 0; c < grid; ++c) {
-        cta_begin[c] = (uint32_t)items.size();
-        for (size_t t = c; t < order.size(); t += grid)
-            items.push_back(order[t]);
+    list_begin.assign(lists + 1, 0);
+    for (int l = 0; l < lists; ++l) {
+        list_begin[l] = (uint32_t)items.size();
+        items.insert(items.end(), per[l].begin(), per[l].end());
     }
-    cta_begin[grid] = (uint32_t)items.size();
+    list_begin[lists] = (uint32_t)items.size();
 }
 
 // Caller holds g_mu.
-int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs, int block_n, int stages,
-              int max_ctas, cudaStream_t stream, CachedTable **out)
+int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stages, int grid_cap,
+              cudaStream_t stream, CachedTable **out)
 {
     std::vector<uint8_t> sig(sizeof(int) * 4 + gs.size() * sizeof(ActiveGroup));
-    int hdr[4] = {dev, block_n, stages, max_ctas};
+    int hdr[4] = {dev, block_n, stages, grid_cap};
     memcpy(sig.data(), hdr, sizeof(hdr));
     if (!gs.empty())
         memcpy(sig.data() + sizeof(hdr), gs.data(), gs.size() * sizeof(ActiveGroup));
@@ -243,12 +260,11 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     std::vector<WorkItem> items;
     std::vector<uint32_t> cta_begin;
     int grid = 0;
-    const int cap = max_ctas > 0 ? std::min(max_ctas, ds.sm_count) : ds.sm_count;
-    build_schedule(gs, block_n, cap, items, cta_begin, grid);
+    build_schedule(gs, block_n, grid_cap, items, cta_begin, grid);
 
     const size_t off_groups = sizeof(TableHeader);
     const size_t off_cta = off_groups + gs.size() * sizeof(GroupEntry);
-    const size_t off_items = (off_cta + (grid + 1) * sizeof(uint32_t) + 15) & ~size_t(15);
+    const size_t off_items = (off_cta + cta_begin.size() * sizeof(uint32_t) + 15) & ~size_t(15);
     const size_t total = off_items + items.size() * sizeof(WorkItem);
 
     CachedTable t;
@@ -324,8 +340,10 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     return NVFP4_OK;
 }
 
+// Sets the kernel's shared-memory limit once per device and checks that one CTA
+// fits on an SM.
 template <int BN, int STAGES>
-int launch_gemm(DeviceState &ds, const CachedTable &t, int nslot, cudaStream_t stream, int num_groups)
+int prepare_kernel(DeviceState &ds, int nslot)
 {
     using L = Layout<BN, STAGES>;
     auto kern = nvfp4_grouped_gemm_kernel<BN, STAGES>;
@@ -333,15 +351,28 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, int nslot, cudaStream_t s
         return NVFP4_ERR_UNSUPPORTED_DEVICE;
     if (!ds.attr_set[nslot]) {
         CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes));
+        int n = 0;
+        CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, L::kSmemBytes));
+        if (n < 1)
+            return NVFP4_ERR_UNSUPPORTED_DEVICE;
         ds.attr_set[nslot] = true;
     }
+    return NVFP4_OK;
+}
+
+template <int BN, int STAGES>
+int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
+{
+    using L = Layout<BN, STAGES>;
     KernelArgs args{};
     args.table = static_cast<const Table *>(t.dev);
     args.status = ds.status;
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
     args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
     args.num_groups = num_groups;
-    kern<<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
+    args.prefetch_stages = (int32_t)(g_opt.prefetch_stages.load() < 0 ? kDefaultPrefetchStages
+                                                                       : g_opt.prefetch_stages.load());
+    nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;
 }
@@ -382,12 +413,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
             return rc;
 
     const int64_t opt_bn = g_opt.block_n.load(), opt_st = g_opt.stages.load();
-    const int block_n = 128;
-    if (opt_bn != 0 && opt_bn != 128)
-        return NVFP4_ERR_INVALID_ARG;
-    const int stages = opt_st == 0 ? 6 : (int)opt_st;
-    if (stages != 2 && stages != 4 && stages != 6)
-        return NVFP4_ERR_INVALID_ARG;
+    const int block_n = opt_bn == 0 ? kDefaultBlockN : (int)opt_bn;
+    const bool shallow = opt_st == 2;
 
     std::lock_guard<std::mutex> lock(g_mu);
     int dev = 0;
@@ -442,13 +469,28 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         CUDA_TRY(launch_prepack(jobs.data(), (int)jobs.size(), stream));
     }
 
-    CachedTable *t = nullptr;
-    if (int rc = get_table(dev, *ds, gs, block_n, stages, (int)g_opt.max_ctas.load(), stream, &t))
+    const int variant = (block_n == 256 ? 2 : 0) + (shallow ? 1 : 0);
+    int rc = NVFP4_OK;
+    switch (variant) {
+    case 0: rc = prepare_kernel<128, kDeepStages128>(*ds, 0); break;
+    case 1: rc = prepare_kernel<128, 2>(*ds, 1); break;
+    case 2: rc = prepare_kernel<256, kDeepStages256>(*ds, 2); break;
+    default: rc = prepare_kernel<256, 2>(*ds, 3); break;
+    }
+    if (rc)
         return rc;
-    switch (stages) {
-    case 2: return launch_gemm<128, 2>(*ds, *t, 0, stream, (int)gs.size());
-    case 4: return launch_gemm<128, 4>(*ds, *t, 1, stream, (int)gs.size());
-    default: return launch_gemm<128, 6>(*ds, *t, 2, stream, (int)gs.size());
+    const int64_t max_ctas = g_opt.max_ctas.load();
+    int grid_cap = ds->sm_count;
+    if (max_ctas > 0)
+        grid_cap = (int)std::min<int64_t>(max_ctas, grid_cap);
+    CachedTable *t = nullptr;
+    if (int rc2 = get_table(dev, gs, block_n, variant, grid_cap, stream, &t))
+        return rc2;
+    switch (variant) {
+    case 0: return launch_gemm<128, kDeepStages128>(*ds, *t, stream, (int)gs.size());
+    case 1: return launch_gemm<128, 2>(*ds, *t, stream, (int)gs.size());
+    case 2: return launch_gemm<256, kDeepStages256>(*ds, *t, stream, (int)gs.size());
+    default: return launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size());
     }
 }
 
@@ -526,12 +568,12 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
 {
     switch (option) {
     case NVFP4_OPT_BLOCK_N:
-        if (value != 0 && value != 128)
+        if (value != 0 && value != 128 && value != 256)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.block_n = value;
         return NVFP4_OK;
     case NVFP4_OPT_STAGES:
-        if (value != 0 && value != 2 && value != 4 && value != 6)
+        if (value != 0 && value != 2)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.stages = value;
         return NVFP4_OK;
@@ -544,6 +586,11 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         if (value < 1 || value > 60000000)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.timeout_us = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_PREFETCH_STAGES:
+        if (value < -1 || value > 64)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.prefetch_stages = value;
         return NVFP4_OK;
     case NVFP4_OPT_FAULT_SKIP_LOAD:
         if (value < -1)
@@ -649,13 +696,14 @@ int noalloc_setup(int dev, NoAllocDevice **out)
         CUDA_TRY(cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev));
         CUDA_TRY(cudaDeviceGetAttribute(&d.sm_count, cudaDevAttrMultiProcessorCount, dev));
         CUDA_TRY(cudaDeviceGetAttribute(&smem, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev));
-        d.supported = (major == 10 && minor == 3) && smem >= Layout<128, 6>::kSmemBytes;
+        d.supported = (major == 10 && minor == 3) && smem >= Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes;
         if (d.supported) {
             void *p = nullptr;
             CUDA_TRY(cudaGetSymbolAddress(&p, g_noalloc_scratch));
             d.scratch = static_cast<uint8_t *>(p);
-            CUDA_TRY(cudaFuncSetAttribute(nvfp4_grouped_gemm_kernel<128, 6>,
-                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<128, 6>::kSmemBytes));
+            CUDA_TRY(cudaFuncSetAttribute(nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages>,
+                                          cudaFuncAttributeMaxDynamicSharedMemorySize, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes));
+
         }
         d.ready = true;
     }
@@ -684,7 +732,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     }
 
     // Size the table before touching anything.
-    constexpr int BN = 128;
+    constexpr int BN = kDefaultBlockN;
     size_t ngroups = 0, ntiles = 0;
     for (int i = 0; i < g; ++i) {
         const Nvfp4Problem &p = probs[i];
@@ -705,7 +753,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     const int grid = (int)std::max<size_t>(1, std::min<size_t>(ntiles, (size_t)cap));
     const size_t off_groups = sizeof(TableHeader);
     const size_t off_cta = off_groups + ngroups * sizeof(GroupEntry);
-    const size_t off_items = (off_cta + (size_t)(grid + 1) * sizeof(uint32_t) + 15) & ~size_t(15);
+    const int lists = grid * kPipes;
+    const size_t off_items = (off_cta + (size_t)(lists + 1) * sizeof(uint32_t) + 15) & ~size_t(15);
     const size_t total = off_items + ntiles * sizeof(WorkItem);
     if (total > kNoAllocScratchBytes - kNoAllocStatusBytes)
         return NVFP4_ERR_TOO_LARGE;
@@ -737,14 +786,16 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     GroupEntry *ge = reinterpret_cast<GroupEntry *>(h + off_groups);
     uint32_t *cta_begin = reinterpret_cast<uint32_t *>(h + off_cta);
     WorkItem *items = reinterpret_cast<WorkItem *>(h + off_items);
-    // CTA c holds tiles c, c + grid, c + 2*grid, ...: it gets ceil((ntiles - c) / grid)
-    // of them, and tile t sits at slot cta_begin[t % grid] + t / grid.
+    // Tile t goes to list l = (t % grid) * kPipes + (t / grid) % kPipes (the cached
+    // path's rule). List l = c * kPipes + p holds t = c + grid * (kPipes * j + p) for
+    // j = 0, 1, ..., so tile t sits at position t / (kPipes * grid) of its list.
     uint32_t run = 0;
-    for (int c = 0; c < grid; ++c) {
-        cta_begin[c] = run;
-        run += (ntiles > (size_t)c) ? (uint32_t)((ntiles - c + grid - 1) / grid) : 0u;
+    for (int l = 0; l < lists; ++l) {
+        const size_t first = (size_t)(l / kPipes) + (size_t)grid * (l % kPipes);
+        cta_begin[l] = run;
+        run += (ntiles > first) ? (uint32_t)((ntiles - first + (size_t)kPipes * grid - 1) / ((size_t)kPipes * grid)) : 0u;
     }
-    cta_begin[grid] = run;
+    cta_begin[lists] = run;
     int gi = 0;
     size_t t = 0;
     for (int i = 0; i < g; ++i) {
@@ -768,7 +819,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         e.tiles_n = (p.N + BN - 1) / BN;
         for (int n = 0; n < e.tiles_n; ++n)
             for (int m = 0; m < e.tiles_m; ++m, ++t)
-                items[cta_begin[t % grid] + t / grid] = WorkItem{gi, m, n, 0};
+                items[cta_begin[list_of_tile(t, grid)] + t / ((size_t)kPipes * grid)] = WorkItem{gi, m, n, 0};
         ++gi;
     }
 
@@ -786,7 +837,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
     args.fault_skip_load = -1;
     args.num_groups = (int32_t)ngroups;
-    nvfp4_grouped_gemm_kernel<128, 6><<<grid, kThreads, Layout<128, 6>::kSmemBytes, stream>>>(args);
+    args.prefetch_stages = kDefaultPrefetchStages;
+    nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;
 }

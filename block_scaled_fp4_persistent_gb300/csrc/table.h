@@ -70,6 +70,7 @@ struct KernelArgs {
     uint64_t timeout_ns;    // bound of every wait
     int32_t fault_skip_load;  // -1 off; else CTA 0 skips the copies of that k-stage
     int32_t num_groups;
+    int32_t prefetch_stages;  // L2 prefetch distance of the producer, in stages (0 = none)
 };
 
 }  // namespace nvfp4

@@ -133,9 +133,14 @@ int nvfp4_last_cuda_error(void);
 
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
- *  NVFP4_OPT_BLOCK_N       : 0 = automatic, or 128
- *  NVFP4_OPT_STAGES        : 0 = automatic, or 2..6 (shared-memory ring depth)
- *  NVFP4_OPT_MAX_CTAS      : 0 = one per SM, or an upper bound on the grid
+ *  NVFP4_OPT_BLOCK_N       : 0 = automatic (128), or 128 or 256: the width of
+ *                             the output tiles (and the MMA's N)
+ *  NVFP4_OPT_STAGES        : 0 = automatic (the deepest shared-memory ring that
+ *                             fits: 6 stages at BLOCK_N 128, 4 at 256), or 2
+ *  NVFP4_OPT_MAX_CTAS      : 0 = one CTA per SM, or an upper bound on the grid
+ *  NVFP4_OPT_PREFETCH_STAGES: -1 = automatic (0), or 0..64: how many K-stages
+ *                             ahead of its shared-memory ring each CTA prefetches
+ *                             its operands into L2
  *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
  *                             (default 2,000,000 us)
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
@@ -149,7 +154,8 @@ enum {
     NVFP4_OPT_STAGES = 2,
     NVFP4_OPT_MAX_CTAS = 3,
     NVFP4_OPT_WAIT_TIMEOUT_US = 4,
-    NVFP4_OPT_FAULT_SKIP_LOAD = 5
+    NVFP4_OPT_FAULT_SKIP_LOAD = 5,
+    NVFP4_OPT_PREFETCH_STAGES = 6
 };
 int nvfp4_set_option(int option, int64_t value);
 

@@ -92,13 +92,16 @@ def test_structured_closed_form():
         assert np.all(dg.result().astype(np.float64) == g.K)
 
 
-@pytest.mark.parametrize("stages", [2, 4, 6])
+@pytest.mark.parametrize("block_n", [128, 256])
+@pytest.mark.parametrize("stages", [2, 0])
 @pytest.mark.parametrize("max_ctas", [1, 3, 0])
-def test_pipeline_depth_and_grid_do_not_change_results(stages, max_ctas):
+def test_tile_width_depth_and_grid_do_not_change_results(block_n, stages, max_ctas):
     groups = gen.make_problem_set(5, [200, 64, 129], [384, 256, 136], [1536, 512, 768])
+    nv.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, block_n)
     base = [DeviceGroup(g) for g in groups]
     run(base)
-    check_full(groups, base, "baseline") if (stages, max_ctas) == (6, 0) else None
+    if (stages, max_ctas) == (0, 0):
+        check_full(groups, base, f"block_n={block_n}")
     nv.nvfp4_set_option(nv.NVFP4_OPT_STAGES, stages)
     nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, max_ctas)
     d = [DeviceGroup(g) for g in groups]
@@ -106,6 +109,15 @@ def test_pipeline_depth_and_grid_do_not_change_results(stages, max_ctas):
     for a, b in zip(base, d):
         assert np.array_equal(a.result().view(np.uint16), b.result().view(np.uint16))
         assert b.guards_intact()
+
+
+@pytest.mark.parametrize("block_n", [128, 256])
+def test_ragged_shapes_both_tile_widths(block_n):
+    nv.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, block_n)
+    groups = gen.make_problem_set(RAGGED["seed"] + 1, RAGGED["Ms"], RAGGED["Ns"], RAGGED["Ks"])
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    check_full(groups, d, f"ragged block_n={block_n}")
 
 
 # --------------------------------------------------------------- edge cases ---
