@@ -39,6 +39,8 @@ NVFP4_OPT_MAX_CTAS = 3
 NVFP4_OPT_WAIT_TIMEOUT_US = 4
 NVFP4_OPT_FAULT_SKIP_LOAD = 5
 NVFP4_OPT_PREFETCH_STAGES = 6
+NVFP4_OPT_SPLIT_TAIL = 7
+NVFP4_OPT_CTA_PAIR = 8
 
 
 class Nvfp4Error(RuntimeError):

@@ -78,7 +78,7 @@ struct Layout {
     static constexpr int kRingBytes = STAGES * kStageBytes;
     // barriers: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain, then the TMEM base word
     static constexpr int kBarBytes = (3 * STAGES + 3) * 8 + 16;
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + 64;
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + 64;  // the SharedState lives in the last 64
     // TMEM columns: the accumulator at 0 .. BN-1, then one scale slot per stage:
     //   SFA at +0 .. 15 (k-block j at +4j),
     //   SFB at +16 .. (k-block j at +16 + 4*kHalves*j; its half h at +4h within that).
@@ -91,6 +91,7 @@ struct Layout {
 
 struct SharedState {
     volatile int abort;  // set by the first role that gives up a wait
+    volatile int last;   // epilogue: this CTA completes the split tile being stored
 };
 
 // Records the first error of the launch in the device status words.
@@ -224,7 +225,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             struct Src {  // where one tile's stages come from
                 const void *tmap_a, *tmap_b;
                 int32_t ya, yb;
-                int kb64, nk;
+                int kb64, kb_begin, kb_end;
                 bool b_shared;
                 const uint8_t *sfa;
                 const uint8_t *sfb[L::kHalves];
@@ -238,7 +239,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 r.ya = w.tile_m * kBlockM;
                 r.yb = w.tile_n * BN;
                 r.kb64 = ge.kblocks64;
-                r.nk = (r.kb64 + 3) / 4;
+                r.kb_begin = w.kb_begin;
+                r.kb_end = w.kb_end;
                 r.b_shared = ge.tiles_m > 1;
                 r.sfa = ge.sfa + (size_t)w.tile_m * r.kb64 * kScaleBlockBytes;
                 // The scales of B come in 128-row tiles. A half of the B tile that lies
@@ -254,10 +256,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             };
             // prefetch cursor
             uint32_t pf_it = item_begin, pf_g = 0;
-            int pf_kb = 0;
             Src pf{};
             if (pf_it < item_end)
                 pf = source(pf_it);
+            int pf_kb = pf.kb_begin;
             auto prefetch_until = [&](uint32_t g_end) {
                 while (pf_g < g_end && pf_it < item_end) {
                     const uint32_t sfb_bytes = (uint32_t)min(4, pf.kb64 - pf_kb * 4) * kScaleBlockBytes;
@@ -268,10 +270,11 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     for (int h = 0; h < L::kHalves; ++h)
                         bulk_prefetch(pf.sfb[h] + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
                     ++pf_g;
-                    if (++pf_kb == pf.nk) {
-                        pf_kb = 0;
-                        if (++pf_it < item_end)
+                    if (++pf_kb == pf.kb_end) {
+                        if (++pf_it < item_end) {
                             pf = source(pf_it);
+                            pf_kb = pf.kb_begin;
+                        }
                     }
                 }
             };
@@ -281,7 +284,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const Src src = source(it);
                 const uint64_t pol_b = src.b_shared ? pol_b_shared : pol_b_stream;
-                for (int kb = 0; kb < src.nk; ++kb, ++kiter) {
+                for (int kb = src.kb_begin; kb < src.kb_end; ++kb, ++kiter) {
                     if (pf_dist > 0)
                         prefetch_until(kiter + pf_dist);
                     if (!wait_phase(smem_addr(&empty[stage]), phase ^ 1u, sh, args, kRoleProducer, (int)it, kb)) {
@@ -335,7 +338,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = tab->item(it);
                 const int kb64 = tab->group(w.group).kblocks64;
-                const int nk = (kb64 + 3) / 4;
                 // the epilogue warps must have drained the previous tile's accumulator
                 if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
                     ok = false;
@@ -343,7 +345,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 }
                 acc_phase ^= 1u;
                 tc_fence_after();
-                for (int kb = 0; kb < nk; ++kb) {
+                for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                     // sf_full is released by the stagers only after they acquired the
                     // stage's full barrier, so the TMA writes of A and B are ordered
                     // before this wait.
@@ -352,7 +354,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t acc0 = kb > 0 ? 1u : 0u;
+                    const uint32_t acc0 = kb > w.kb_begin ? 1u : 0u;
                     if (kb64 - kb * 4 >= 4) {
                         // K step of 64 E2M1 = 32 bytes inside the 128-byte swizzled row: +2 in the
                         // descriptor's 16-byte address field
@@ -399,9 +401,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         bool ok = true;
         for (uint32_t it = item_begin; ok && it < item_end; ++it) {
             const WorkItem w = tab->item(it);
-            const int kb64 = tab->group(w.group).kblocks64;
-            const int nk = (kb64 + 3) / 4;
-            for (int kb = 0; kb < nk; ++kb) {
+            for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                 if (!warp_wait_phase(smem_addr(&full[stage]), phase, sh, args, kRoleScales, (int)it, kb)) {
                     ok = false;
                     break;
@@ -460,32 +460,102 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 break;
             acc_phase ^= 1u;
             tc_fence_after();
-            // drain: 32 columns at a time, packed to fp16 pairs as they arrive
-            uint32_t hv[kCols / 2];
-#pragma unroll
-            for (int c = 0; c < kCols / 32; ++c) {
-                uint32_t v[32];
-                tmem_load_32cols(t_addr + c * 32, v);
-                tmem_load_wait();
-                reg_fence(v);
-#pragma unroll
-                for (int i = 0; i < 16; ++i)
-                    hv[c * 16 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
-            }
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0)
-                mbar_arrive(smem_addr(acc_empty));
             const int m = w.tile_m * kBlockM + row_in_tile;
             const int n0 = w.tile_n * BN + chalf * kCols;
-            if (m < M) {
-                __half *crow = C + (size_t)m * N + n0;
+            if (w.split < 0) {
+                // whole tile: drain 32 columns at a time, packed to fp16 pairs as they arrive
+                uint32_t hv[kCols / 2];
 #pragma unroll
-                for (int q = 0; q < kCols / 8; ++q) {
-                    if (n0 + q * 8 < N)
-                        *reinterpret_cast<uint4 *>(crow + q * 8) =
-                            make_uint4(hv[4 * q + 0], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                for (int c = 0; c < kCols / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_load_32cols(t_addr + c * 32, v);
+                    tmem_load_wait();
+                    reg_fence(v);
+#pragma unroll
+                    for (int i = 0; i < 16; ++i)
+                        hv[c * 16 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
                 }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(acc_empty));
+                if (m < M) {
+                    __half *crow = C + (size_t)m * N + n0;
+#pragma unroll
+                    for (int q = 0; q < kCols / 8; ++q) {
+                        if (n0 + q * 8 < N)
+                            *reinterpret_cast<uint4 *>(crow + q * 8) =
+                                make_uint4(hv[4 * q + 0], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                    }
+                }
+            } else {
+                // one segment of a split tile: its fp32 partial goes to the workspace slot.
+                // Thread e of the epilogue keeps its elements at float4 index (c*8 + f)*256 + e
+                // of the slot, so every store and load of a warp covers 512 contiguous bytes.
+                const int e = (warp - kEpilogueWarp0) * 32 + (int)lane;
+                constexpr int kSlotFloats = kBlockM * BN;
+                float4 *ws = reinterpret_cast<float4 *>(args.workspace + (size_t)w.ws_slot * kSlotFloats);
+#pragma unroll
+                for (int c = 0; c < kCols / 32; ++c) {
+                    uint32_t v[32];
+                    tmem_load_32cols(t_addr + c * 32, v);
+                    tmem_load_wait();
+                    reg_fence(v);
+#pragma unroll
+                    for (int f = 0; f < 8; ++f)
+                        ws[(c * 8 + f) * 256 + e] = make_float4(__uint_as_float(v[4 * f + 0]), __uint_as_float(v[4 * f + 1]),
+                                                                __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(acc_empty));
+                // Count this segment in. The segment that completes the count sums all of
+                // them; nothing ever waits for another CTA.
+                __threadfence();
+                named_barrier_sync(1, kEpilogueWarps * 32);
+                if (e == 0)
+                    sh->last = (atomicAdd(&args.counters[w.split], 1) == w.nseg - 1) ? 1 : 0;
+                named_barrier_sync(1, kEpilogueWarps * 32);
+                if (sh->last) {
+                    __threadfence();
+                    const float4 *ws0 = reinterpret_cast<const float4 *>(args.workspace +
+                                                                         (size_t)(w.ws_slot - w.seg) * kSlotFloats);
+                    if (m < M) {
+                        __half *crow = C + (size_t)m * N + n0;
+#pragma unroll 1
+                        for (int c = 0; c < kCols / 32; ++c) {
+                            // 32 columns at a time, eight independent loads per segment in
+                            // flight; segments are added in K order, so the rounding does not
+                            // depend on which segment finished last
+                            float4 acc[8];
+#pragma unroll
+                            for (int f = 0; f < 8; ++f)
+                                acc[f] = __ldcg(&ws0[(c * 8 + f) * 256 + e]);
+                            for (int sg = 1; sg < w.nseg; ++sg) {
+                                const float4 *wp = ws0 + (size_t)sg * (kSlotFloats / 4);
+                                float4 q[8];
+#pragma unroll
+                                for (int f = 0; f < 8; ++f)
+                                    q[f] = __ldcg(&wp[(c * 8 + f) * 256 + e]);
+#pragma unroll
+                                for (int f = 0; f < 8; ++f)
+                                    acc[f].x += q[f].x, acc[f].y += q[f].y, acc[f].z += q[f].z, acc[f].w += q[f].w;
+                            }
+#pragma unroll
+                            for (int f = 0; f < 8; ++f) {
+                                const int col = c * 32 + f * 4;
+                                if (n0 + col < N)
+                                    *reinterpret_cast<uint2 *>(crow + col) =
+                                        make_uint2(pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y)),
+                                                   pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w)));
+                            }
+                        }
+                    }
+                    if (e == 0)
+                        args.counters[w.split] = 0;  // ready for the next launch
+                }
+                named_barrier_sync(1, kEpilogueWarps * 32);  // sh->last is read before it is rewritten
             }
         }
     }

@@ -28,6 +28,7 @@
 
 #include "nvfp4_grouped_gemm.h"
 #include "gemm_kernel.cuh"
+#include "pair_kernel.cuh"
 #include "prepack.cuh"
 #include "table.h"
 
@@ -46,6 +47,8 @@ struct Options {
     std::atomic<int64_t> timeout_us{2000000};
     std::atomic<int64_t> fault_skip_load{-1};
     std::atomic<int64_t> prefetch_stages{-1};  // -1 = automatic
+    std::atomic<int64_t> split_tail{1};
+    std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
 } g_opt;
 
 constexpr int kMaxDevices = 64;
@@ -55,6 +58,10 @@ constexpr int kDefaultBlockN = 128;
 constexpr int kDeepStages128 = 6;  // 6 x 36 KB
 constexpr int kDeepStages256 = 4;  // 4 x 54 KB
 constexpr int kDefaultStages = kDefaultBlockN == 256 ? kDeepStages256 : kDeepStages128;
+// The CTA-pair kernel: 256 x 256 tiles, 5 x 38 KB ring (its TMEM holds 5 scale slots).
+constexpr int kPairStages = 5;
+constexpr int kVariantPair = 4;
+constexpr int kVariantAuto = -1;  // chosen per problem set: CTA pairs or single CTAs with 128 x 128 tiles
 // How far ahead of the ring the producer prefetches into L2, in stages.
 constexpr int kDefaultPrefetchStages = 0;
 constexpr int kMaxDim = 1 << 24;
@@ -67,6 +74,7 @@ struct DeviceState {
     int max_smem_optin = 0;
     int *status = nullptr;  // device: 4 words
     bool attr_set[8] = {};
+    int pair_clusters = 0;  // CTA pairs of the pair kernel that fit on the device at once
 };
 
 std::mutex g_mu;  // guards everything below
@@ -76,12 +84,15 @@ struct CachedTable {
     uint64_t key = 0;
     std::vector<uint8_t> signature;  // exact inputs of the table, to rule out hash collisions
     void *dev = nullptr;
+    float *workspace = nullptr;      // fp32 partials of split tiles
+    int *counters = nullptr;         // one per split tile, 0 between launches
+    int splits = 0;
     void *host = nullptr;  // pinned copy, kept alive for the asynchronous upload
     size_t bytes = 0;
     int device = 0;
     int grid = 0;
     int block_n = 0;
-    int stages = 0;
+    int variant = 0;  // the kernel variant the table was built for
 };
 std::list<CachedTable> g_tables;  // most recently used first
 std::unordered_map<uint64_t, std::list<CachedTable>::iterator> g_table_index;
@@ -175,6 +186,24 @@ int encode_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, u
     return NVFP4_OK;
 }
 
+// The fp16 output [M][N] as 32 x 32 boxes (64 bytes per box row) with the
+// 64-byte swizzle, for TMA stores from the epilogue's staging buffers.
+int encode_output_map(CUtensorMap *map, void *C, uint64_t M, uint64_t N)
+{
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * 2};
+    cuuint32_t box[2] = {32, 32};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_64B, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error.store(10000 + (int)r);
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
 int check_problem(const Nvfp4Problem &p)
 {
     if (p.M < 0 || p.N < 0 || p.K < 0)
@@ -214,36 +243,155 @@ struct ActiveGroup {
 // once and from L2 after that. Each SM's two pipelines take alternate waves.
 inline int list_of_tile(size_t t, int grid) { return (int)(t % grid) * kPipes + (int)((t / grid) % kPipes); }
 
-void build_schedule(const std::vector<ActiveGroup> &gs, int block_n, int grid_cap, std::vector<WorkItem> &items,
-                    std::vector<uint32_t> &list_begin, int &grid)
+struct Schedule {
+    std::vector<WorkItem> items;
+    std::vector<uint32_t> list_begin;
+    int grid = 0;
+    int splits = 0;    // split tiles (one counter each)
+    int ws_slots = 0;  // fp32 partial slots (one per segment of a split tile)
+};
+
+// Tiles are numbered group by group, and inside a group B-strip by B-strip
+// (tile_n outer, tile_m inner), so that the CTAs running at the same moment
+// hold neighbouring tiles: the m-tiles that share one strip of B read it from
+// HBM once and from L2 after that.
+//
+// Balance. When every tile has the same number of K-stages and there are more
+// tiles than CTAs, the first floor(T/G)*G tiles go round-robin, whole. The
+// remaining T mod G tiles (the tail) are cut along K so that every CTA gets the
+// same number of tail stages: CTA c takes stages [c*W/G, (c+1)*W/G) of the
+// tail's W stages. A tail tile that lands on several CTAs is a split tile: its
+// segments write fp32 partials and the last to finish stores C. Otherwise (mixed
+// K, T <= G, or split_tail off) every tile goes whole to CTA t % G.
+Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int block_n, int grid_cap, bool split_tail)
 {
-    std::vector<WorkItem> order;
+    struct Tile {
+        int group, m, n, nk;
+    };
+    std::vector<Tile> tiles;
     for (int gi = 0; gi < (int)gs.size(); ++gi) {
-        const int tm = (gs[gi].M + kBlockM - 1) / kBlockM, tn = (gs[gi].N + block_n - 1) / block_n;
+        const int tm = (gs[gi].M + block_m - 1) / block_m, tn = (gs[gi].N + block_n - 1) / block_n;
+        const int nk = (gs[gi].K / 64 + 3) / 4;
         for (int n = 0; n < tn; ++n)
             for (int m = 0; m < tm; ++m)
-                order.push_back(WorkItem{gi, m, n, 0});
+                tiles.push_back(Tile{gi, m, n, nk});
     }
-    grid = std::max(1, std::min<int>((int)order.size(), grid_cap));
-    const int lists = grid * kPipes;
-    std::vector<std::vector<WorkItem>> per(lists);
-    for (size_t t = 0; t < order.size(); ++t)
-        per[list_of_tile(t, grid)].push_back(order[t]);
-    items.clear();
-    list_begin.assign(lists + 1, 0);
+    Schedule sc;
+    const size_t T = tiles.size();
+    sc.grid = std::max(1, std::min<int>((int)T, grid_cap));
+    const int G = sc.grid, lists = G * kPipes;
+    bool uniform = true;
+    for (const Tile &t : tiles)
+        uniform = uniform && t.nk == tiles[0].nk;
+    size_t whole = T;
+    if (split_tail && uniform && T > (size_t)G && T % G != 0) {
+        // Split only where it shortens the busiest CTA by at least an eighth (and two
+        // stages): each split costs a partial write and a reduction.
+        const int64_t nk = tiles[0].nk;
+        const int64_t unbalanced = (int64_t)((T + G - 1) / G) * nk;
+        const int64_t balanced = ((int64_t)T * nk + G - 1) / G;
+        if (unbalanced - balanced >= 2 && (unbalanced - balanced) * 8 >= unbalanced)
+            whole = (T / G) * G;
+    }
+    // Split segments go at the head of their CTA's list: their partial writes and
+    // reductions then overlap the whole tiles that follow instead of ending the launch.
+    std::vector<std::vector<WorkItem>> head(lists), per(lists);
+    for (size_t t = 0; t < whole; ++t) {
+        const Tile &x = tiles[t];
+        per[list_of_tile(t, G)].push_back(WorkItem{x.group, x.m, x.n, 0, x.nk, -1, 0, 1, 0, {0, 0, 0}});
+    }
+    if (whole < T) {
+        const int nk = tiles[0].nk;
+        const int64_t W = (int64_t)(T - whole) * nk;
+        auto cta_start = [&](int c) { return (int64_t)c * W / G; };
+        for (size_t r = 0; r < T - whole; ++r) {
+            const Tile &x = tiles[whole + r];
+            const int64_t a = (int64_t)r * nk, b = a + nk;
+            // CTAs whose tail ranges meet [a, b)
+            int c0 = (int)std::min<int64_t>(G - 1, a * G / W);
+            while (c0 > 0 && cta_start(c0) > a)
+                --c0;
+            while (cta_start(c0 + 1) <= a)
+                ++c0;
+            std::vector<std::pair<int, std::pair<int, int>>> segs;  // cta, [kb_begin, kb_end)
+            for (int c = c0; c < G && cta_start(c) < b; ++c) {
+                const int64_t lo = std::max(a, cta_start(c)), hi = std::min(b, cta_start(c + 1));
+                if (hi > lo)
+                    segs.push_back({c, {(int)(lo - a), (int)(hi - a)}});
+            }
+            const int nseg = (int)segs.size();
+            const int split = nseg > 1 ? sc.splits++ : -1;
+            for (int j = 0; j < nseg; ++j) {
+                const int slot = nseg > 1 ? sc.ws_slots++ : 0;
+                head[segs[j].first * kPipes].push_back(
+                    WorkItem{x.group, x.m, x.n, segs[j].second.first, segs[j].second.second, split, j, nseg, slot, {0, 0, 0}});
+            }
+        }
+    }
+    sc.list_begin.assign(lists + 1, 0);
     for (int l = 0; l < lists; ++l) {
-        list_begin[l] = (uint32_t)items.size();
-        items.insert(items.end(), per[l].begin(), per[l].end());
+        sc.list_begin[l] = (uint32_t)sc.items.size();
+        sc.items.insert(sc.items.end(), head[l].begin(), head[l].end());
+        sc.items.insert(sc.items.end(), per[l].begin(), per[l].end());
     }
-    list_begin[lists] = (uint32_t)items.size();
+    sc.list_begin[lists] = (uint32_t)sc.items.size();
+    return sc;
 }
 
-// Caller holds g_mu.
-int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stages, int grid_cap,
-              cudaStream_t stream, CachedTable **out)
+// How one kernel variant tiles a problem set.
+struct Plan {
+    int variant;
+    int block_m, block_n;
+    int grid_cap;  // lists: CTAs, or CTA pairs
+};
+
+Plan plan_for(int variant, const DeviceState &ds, int64_t max_ctas)
 {
-    std::vector<uint8_t> sig(sizeof(int) * 4 + gs.size() * sizeof(ActiveGroup));
-    int hdr[4] = {dev, block_n, stages, grid_cap};
+    const bool pair = variant == kVariantPair;
+    Plan p;
+    p.variant = variant;
+    p.block_m = pair ? kPairBlockM : kBlockM;
+    p.block_n = pair ? kPairBlockN : (variant >= 2 ? 256 : 128);
+    int cap = pair ? ds.pair_clusters : ds.sm_count;
+    if (max_ctas > 0)
+        cap = (int)std::min<int64_t>(pair ? std::max<int64_t>(1, max_ctas / 2) : max_ctas, cap);
+    p.grid_cap = cap;
+    return p;
+}
+
+// K-stages of the busiest list.
+int64_t makespan_stages(const Schedule &sc)
+{
+    int64_t worst = 0;
+    for (size_t l = 0; l + 1 < sc.list_begin.size(); ++l) {
+        int64_t sum = 0;
+        for (uint32_t i = sc.list_begin[l]; i < sc.list_begin[l + 1]; ++i)
+            sum += sc.items[i].kb_end - sc.items[i].kb_begin;
+        worst = std::max(worst, sum);
+    }
+    return worst;
+}
+
+// The automatic choice between CTA pairs and single CTAs with 128 x 128 tiles,
+// from each schedule's busiest list. Measured on this GPU: a K-stage takes about
+// 0.35 us on a single CTA (128 x 128 outputs) and 0.40 us on a CTA pair
+// (256 x 256), and a pair reaches its first MMA about 1 us later. So pairs win
+// where they cut the busiest list's stages by more than ~15% plus that microsecond:
+// the MoE-sized problem sets; small ones that leave SMs idle stay on single CTAs.
+int choose_variant(const std::vector<ActiveGroup> &gs, const DeviceState &ds, int64_t max_ctas, bool split_tail)
+{
+    const Plan pp = plan_for(kVariantPair, ds, max_ctas), p1 = plan_for(0, ds, max_ctas);
+    const double t_pair = 1.0 + 0.40 * (double)makespan_stages(build_schedule(gs, pp.block_m, pp.block_n, pp.grid_cap, split_tail));
+    const double t_single = 0.35 * (double)makespan_stages(build_schedule(gs, p1.block_m, p1.block_n, p1.grid_cap, split_tail));
+    return t_pair < t_single ? kVariantPair : 0;
+}
+
+// Caller holds g_mu. variant_req is a kernel variant or kVariantAuto.
+int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs, int variant_req, int64_t max_ctas,
+              bool split_tail, cudaStream_t stream, CachedTable **out)
+{
+    std::vector<uint8_t> sig(sizeof(int) * 5 + gs.size() * sizeof(ActiveGroup));
+    int hdr[5] = {dev, variant_req, (int)std::min<int64_t>(max_ctas, 1 << 30), 0, split_tail ? 1 : 0};
     memcpy(sig.data(), hdr, sizeof(hdr));
     if (!gs.empty())
         memcpy(sig.data() + sizeof(hdr), gs.data(), gs.size() * sizeof(ActiveGroup));
@@ -257,10 +405,16 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
     if (int rc = get_encoder())
         return rc;
 
-    std::vector<WorkItem> items;
-    std::vector<uint32_t> cta_begin;
-    int grid = 0;
-    build_schedule(gs, block_n, grid_cap, items, cta_begin, grid);
+    // The pair kernel (variant kVariantPair) runs 256 x 256 tiles, one list per CTA pair.
+    const int variant = variant_req == kVariantAuto ? choose_variant(gs, ds, max_ctas, split_tail) : variant_req;
+    const Plan plan = plan_for(variant, ds, max_ctas);
+    const bool pair = variant == kVariantPair;
+    const int block_m = plan.block_m, block_n = plan.block_n;
+    const int halves = pair ? 2 : 1;  // workspace slots and counters per split segment / tile
+    Schedule sc = build_schedule(gs, block_m, block_n, plan.grid_cap, split_tail);
+    const std::vector<WorkItem> &items = sc.items;
+    const std::vector<uint32_t> &cta_begin = sc.list_begin;
+    const int grid = sc.grid;  // lists: CTAs, or CTA pairs
 
     const size_t off_groups = sizeof(TableHeader);
     const size_t off_cta = off_groups + gs.size() * sizeof(GroupEntry);
@@ -272,9 +426,9 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
     t.signature = std::move(sig);
     t.bytes = total;
     t.device = dev;
-    t.grid = grid;
+    t.grid = grid * halves;
     t.block_n = block_n;
-    t.stages = stages;
+    t.variant = variant;
     CUDA_TRY(cudaMallocHost(&t.host, total));
     memset(t.host, 0, total);
     uint8_t *h = static_cast<uint8_t *>(t.host);
@@ -292,7 +446,9 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
         GroupEntry &e = ge[i];
         int rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, (uint64_t)a.M, kBlockM);
         if (!rc)
-            rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, (uint32_t)block_n);
+            rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, pair ? 128u : (uint32_t)block_n);
+        if (!rc && pair)
+            rc = encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
         if (rc) {
             cudaFreeHost(t.host);
             return rc;
@@ -304,7 +460,7 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
         e.N = a.N;
         e.K = a.K;
         e.kblocks64 = a.K / 64;
-        e.tiles_m = (a.M + kBlockM - 1) / kBlockM;
+        e.tiles_m = (a.M + block_m - 1) / block_m;
         e.tiles_n = (a.N + block_n - 1) / block_n;
     }
     memcpy(h + off_cta, cta_begin.data(), cta_begin.size() * sizeof(uint32_t));
@@ -317,8 +473,18 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
         return cuda_fail(e);
     }
     e = cudaMemcpyAsync(t.dev, t.host, total, cudaMemcpyHostToDevice, stream);
+    if (e == cudaSuccess && sc.splits > 0) {
+        e = cudaMalloc(&t.workspace, (size_t)sc.ws_slots * halves * kBlockM * block_n * sizeof(float));
+        if (e == cudaSuccess)
+            e = cudaMalloc(&t.counters, (size_t)sc.splits * halves * sizeof(int));
+        if (e == cudaSuccess)
+            e = cudaMemsetAsync(t.counters, 0, (size_t)sc.splits * halves * sizeof(int), stream);
+        t.splits = sc.splits * halves;
+    }
     if (e != cudaSuccess) {
         cudaFree(t.dev);
+        cudaFree(t.workspace);
+        cudaFree(t.counters);
         cudaFreeHost(t.host);
         return cuda_fail(e);
     }
@@ -328,6 +494,8 @@ int get_table(int dev, const std::vector<ActiveGroup> &gs, int block_n, int stag
         CUDA_TRY(cudaDeviceSynchronize());
         CachedTable &old = g_tables.back();
         cudaFree(old.dev);
+        cudaFree(old.workspace);
+        cudaFree(old.counters);
         cudaFreeHost(old.host);
         g_table_index.erase(old.key);
         g_tables.pop_back();
@@ -372,7 +540,50 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.num_groups = num_groups;
     args.prefetch_stages = (int32_t)(g_opt.prefetch_stages.load() < 0 ? kDefaultPrefetchStages
                                                                        : g_opt.prefetch_stages.load());
+    args.workspace = t.workspace;
+    args.counters = t.counters;
     nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
+    CUDA_TRY(cudaGetLastError());
+    return NVFP4_OK;
+}
+
+// The pair kernel: shared-memory limit, and how many CTA pairs fit at once
+// (clusters must sit inside one GPC, so this can be fewer than SMs / 2).
+int prepare_pair_kernel(DeviceState &ds)
+{
+    using L = PairLayout<kPairStages>;
+    auto kern = nvfp4_pair_gemm_kernel<kPairStages>;
+    if (L::kSmemBytes > ds.max_smem_optin)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (!ds.attr_set[kVariantPair]) {
+        CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes));
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(2 * (unsigned)std::max(1, ds.sm_count / 2));
+        cfg.blockDim = dim3(kThreads);
+        cfg.dynamicSmemBytes = L::kSmemBytes;
+        int n = 0;
+        CUDA_TRY(cudaOccupancyMaxActiveClusters(&n, kern, &cfg));
+        if (n < 1)
+            return NVFP4_ERR_UNSUPPORTED_DEVICE;
+        ds.pair_clusters = n;
+        ds.attr_set[kVariantPair] = true;
+    }
+    return NVFP4_OK;
+}
+
+int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
+{
+    using L = PairLayout<kPairStages>;
+    KernelArgs args{};
+    args.table = static_cast<const Table *>(t.dev);
+    args.status = ds.status;
+    args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
+    args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
+    args.num_groups = num_groups;
+    args.prefetch_stages = 0;
+    args.workspace = t.workspace;
+    args.counters = t.counters;
+    nvfp4_pair_gemm_kernel<kPairStages><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;
 }
@@ -469,28 +680,35 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         CUDA_TRY(launch_prepack(jobs.data(), (int)jobs.size(), stream));
     }
 
-    const int variant = (block_n == 256 ? 2 : 0) + (shallow ? 1 : 0);
+    // BLOCK_N or STAGES select a single-CTA variant; CTA_PAIR forces either kind.
+    const int64_t opt_pair = g_opt.cta_pair.load();
+    const int single = (block_n == 256 ? 2 : 0) + (shallow ? 1 : 0);
+    const int variant_req = opt_pair == 1 ? kVariantPair
+                            : (opt_pair == 2 || opt_bn != 0 || shallow) ? single
+                                                                        : kVariantAuto;
+    if (variant_req == kVariantPair || variant_req == kVariantAuto)
+        if (int rc = prepare_pair_kernel(*ds))  // also learns how many CTA pairs fit at once
+            return rc;
+    CachedTable *t = nullptr;
+    if (int rc2 = get_table(dev, *ds, gs, variant_req, g_opt.max_ctas.load(), g_opt.split_tail.load() != 0, stream, &t))
+        return rc2;
+    const int variant = t->variant;
     int rc = NVFP4_OK;
     switch (variant) {
     case 0: rc = prepare_kernel<128, kDeepStages128>(*ds, 0); break;
     case 1: rc = prepare_kernel<128, 2>(*ds, 1); break;
     case 2: rc = prepare_kernel<256, kDeepStages256>(*ds, 2); break;
-    default: rc = prepare_kernel<256, 2>(*ds, 3); break;
+    case 3: rc = prepare_kernel<256, 2>(*ds, 3); break;
+    default: rc = prepare_pair_kernel(*ds); break;
     }
     if (rc)
         return rc;
-    const int64_t max_ctas = g_opt.max_ctas.load();
-    int grid_cap = ds->sm_count;
-    if (max_ctas > 0)
-        grid_cap = (int)std::min<int64_t>(max_ctas, grid_cap);
-    CachedTable *t = nullptr;
-    if (int rc2 = get_table(dev, gs, block_n, variant, grid_cap, stream, &t))
-        return rc2;
     switch (variant) {
     case 0: return launch_gemm<128, kDeepStages128>(*ds, *t, stream, (int)gs.size());
     case 1: return launch_gemm<128, 2>(*ds, *t, stream, (int)gs.size());
     case 2: return launch_gemm<256, kDeepStages256>(*ds, *t, stream, (int)gs.size());
-    default: return launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size());
+    case 3: return launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size());
+    default: return launch_pair(*ds, *t, stream, (int)gs.size());
     }
 }
 
@@ -539,8 +757,13 @@ extern "C" int nvfp4_device_status(nvfp4_stream_t stream, int *status, int32_t *
     CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
     int words[4] = {0, 0, 0, 0};
     CUDA_TRY(cudaMemcpy(words, ds->status, sizeof(words), cudaMemcpyDeviceToHost));
-    if (words[0] != 0)
+    if (words[0] != 0) {
         CUDA_TRY(cudaMemset(ds->status, 0, sizeof(words)));
+        // A launch that gave up may have left split-tile counters part-way.
+        for (const CachedTable &t : g_tables)
+            if (t.device == dev && t.counters)
+                CUDA_TRY(cudaMemset(t.counters, 0, (size_t)t.splits * sizeof(int)));
+    }
     *status = words[0];
     if (detail)
         for (int i = 0; i < 4; ++i)
@@ -587,6 +810,16 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.timeout_us = value;
         return NVFP4_OK;
+    case NVFP4_OPT_SPLIT_TAIL:
+        if (value != 0 && value != 1)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.split_tail = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_CTA_PAIR:
+        if (value < 0 || value > 2)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.cta_pair = value;
+        return NVFP4_OK;
     case NVFP4_OPT_PREFETCH_STAGES:
         if (value < -1 || value > 64)
             return NVFP4_ERR_INVALID_ARG;
@@ -616,6 +849,8 @@ extern "C" void nvfp4_release(void)
         for (auto it = g_tables.begin(); it != g_tables.end();) {
             if (it->device == d) {
                 cudaFree(it->dev);
+                cudaFree(it->workspace);
+                cudaFree(it->counters);
                 cudaFreeHost(it->host);
                 g_table_index.erase(it->key);
                 it = g_tables.erase(it);
@@ -819,7 +1054,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         e.tiles_n = (p.N + BN - 1) / BN;
         for (int n = 0; n < e.tiles_n; ++n)
             for (int m = 0; m < e.tiles_m; ++m, ++t)
-                items[cta_begin[list_of_tile(t, grid)] + t / ((size_t)kPipes * grid)] = WorkItem{gi, m, n, 0};
+                items[cta_begin[list_of_tile(t, grid)] + t / ((size_t)kPipes * grid)] =
+                    WorkItem{gi, m, n, 0, (p.K / 64 + 3) / 4, -1, 0, 1, 0, {0, 0, 0}};
         ++gi;
     }
 
@@ -838,6 +1074,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.fault_skip_load = -1;
     args.num_groups = (int32_t)ngroups;
     args.prefetch_stages = kDefaultPrefetchStages;
+    args.workspace = nullptr;  // no split tiles here
+    args.counters = nullptr;
     nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;

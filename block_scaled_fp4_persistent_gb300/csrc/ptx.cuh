@@ -26,6 +26,37 @@ __device__ __forceinline__ uint64_t global_timer_ns()
     return t;
 }
 
+// Named barrier among `threads` threads (a multiple of 32) of the CTA.
+__device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
+// ----------------------------------------------------------------- cluster --
+
+// Rank of this CTA in its cluster (0 or 1 for a CTA pair).
+__device__ __forceinline__ uint32_t cluster_rank()
+{
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// Every thread of every CTA of the cluster; orders prior memory operations
+// (release) before later ones (acquire) across the cluster.
+__device__ __forceinline__ void cluster_sync()
+{
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// The shared::cluster address of the object at shared::cta address `addr` in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank)
+{
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(addr), "r"(rank));
+    return r;
+}
+
 // ---------------------------------------------------------------- mbarrier --
 
 __device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count)
@@ -55,6 +86,16 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity)
 __device__ __forceinline__ void mbar_arrive(uint32_t bar)
 {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// Relaxed arrival on a barrier given by its shared::cluster address (a peer CTA's).
+// It orders none of this thread's memory operations: use it only to announce work
+// that has already completed (a tcgen05.wait::st or ::ld that returned, TMA bytes
+// this warp saw land). A release at cluster scope costs about a microsecond per
+// arrival on this GPU, because it waits for the SM's memory operations in flight.
+__device__ __forceinline__ void mbar_arrive_remote_relaxed(uint32_t cluster_bar)
+{
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes)
@@ -104,6 +145,35 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int3
         : "memory");
 }
 
+// 2-D tiled store this CTA's shared memory -> global, tracked in the thread's
+// bulk async-group. Elements of the box outside the tensor are not written.
+__device__ __forceinline__ void tma_store_2d(const void *tmap, int32_t x, int32_t y, uint32_t src)
+{
+    asm volatile("cp.async.bulk.tensor.2d.global.shared::cta.bulk_group [%0, {%1, %2}], [%3];" ::"l"(tmap), "r"(x),
+                 "r"(y), "r"(src)
+                 : "memory");
+}
+
+__device__ __forceinline__ void bulk_commit_group() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+
+// Waits until at most N of this thread's bulk async-groups still read shared memory.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group_read()
+{
+    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(N) : "memory");
+}
+
+// Waits until at most N of this thread's bulk async-groups are incomplete.
+template <int N>
+__device__ __forceinline__ void bulk_wait_group()
+{
+    asm volatile("cp.async.bulk.wait_group %0;" ::"n"(N) : "memory");
+}
+
+// Makes this thread's generic-proxy writes to shared memory visible to the async
+// proxy (a TMA store that reads them).
+__device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
 // Prefetch of a 2-D tile of the tensor map into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y)
 {
@@ -145,6 +215,23 @@ __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols)
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
 }
 
+// The CTA-pair forms: one warp in each CTA of the pair executes them together;
+// both CTAs receive the same TMEM base.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t dst, uint32_t ncols)
+{
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst), "r"(ncols) : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair()
+{
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols)
+{
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
 __device__ __forceinline__ void tc_fence_before()
 {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
@@ -174,6 +261,33 @@ __device__ __forceinline__ void tc_mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, u
             d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
         : "memory");
+}
+
+// The same MMA on a CTA pair (issued by the even CTA): M = 256, rows 0-127 from
+// this CTA and rows 128-255 from the peer. Each CTA holds its own rows of A and
+// half of the N rows of B at the same shared-memory offsets, its own rows' A
+// scales and all N rows' B scales at the same TMEM columns, and receives its own
+// 128 rows of D at d_tmem.
+__device__ __forceinline__ void tc_mma_nvfp4_pair(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                                  uint32_t sfa_tmem, uint32_t sfb_tmem, uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.block16 [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(
+            d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
+        : "memory");
+}
+
+// Arrives once on the barrier at shared::cta offset `bar` in each CTA of `cta_mask`
+// when every tcgen05 operation this thread issued so far (on the pair) has completed.
+__device__ __forceinline__ void tc_commit_pair(uint32_t bar, uint16_t cta_mask)
+{
+    asm volatile("tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+                     bar),
+                 "h"(cta_mask)
+                 : "memory");
 }
 
 // Arrives once on `bar` when every tcgen05 operation this thread issued so far

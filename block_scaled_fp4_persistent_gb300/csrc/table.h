@@ -21,6 +21,7 @@ constexpr int kStatusTimeout = -5;  // NVFP4_ERR_TIMEOUT
 struct alignas(128) GroupEntry {
     CUtensorMap tmap_a;   // uint8 [M][K/2], box 128 B x 128 rows, 128-byte swizzle
     CUtensorMap tmap_b;   // uint8 [N][K/2], box 128 B x BLOCK_N rows, 128-byte swizzle
+    CUtensorMap tmap_c;   // fp16 [M][N], box 32 x 32, 64-byte swizzle (CTA-pair kernel's stores)
     const uint8_t *sfa;   // blocked scales of A: ceil(M/128) x kblocks64 blocks of 512 B
     const uint8_t *sfb;   // blocked scales of B: ceil(N/128) x kblocks64 blocks of 512 B
     __half *C;            // [M][N] fp16
@@ -29,12 +30,26 @@ struct alignas(128) GroupEntry {
     int32_t tiles_m, tiles_n;
 };
 
+// One segment of an output tile: K-stages kb_begin .. kb_end-1 (256 K each).
+// A tile that is not split has one segment covering all its K-stages
+// (split = -1). A split tile has nseg segments on different CTAs; each writes
+// its fp32 partial to workspace slot ws_slot, and the one that finishes last
+// (counted in counters[split]) sums the slots ws_slot - seg .. ws_slot - seg +
+// nseg - 1 in that order and stores C.
 struct WorkItem {
     int32_t group;
     int32_t tile_m;
     int32_t tile_n;
-    int32_t reserved;
+    int32_t kb_begin;
+    int32_t kb_end;
+    int32_t split;
+    int32_t seg;
+    int32_t nseg;
+    int32_t ws_slot;
+    int32_t reserved[3];
 };
+
+static_assert(sizeof(WorkItem) == 48, "WorkItem is read as three int4");
 
 struct alignas(128) TableHeader {
     int32_t num_groups;
@@ -58,8 +73,9 @@ struct Table {
     }
     __host__ __device__ WorkItem item(uint32_t i) const
     {
-        const int4 v = reinterpret_cast<const int4 *>(reinterpret_cast<const char *>(this) + h.off_items)[i];
-        return WorkItem{v.x, v.y, v.z, v.w};
+        const int4 *p = reinterpret_cast<const int4 *>(reinterpret_cast<const char *>(this) + h.off_items) + 3 * i;
+        const int4 a = p[0], b = p[1], c = p[2];
+        return WorkItem{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, {0, 0, 0}};
     }
     int num_groups_host() const { return h.num_groups; }
 };
@@ -71,6 +87,8 @@ struct KernelArgs {
     int32_t fault_skip_load;  // -1 off; else CTA 0 skips the copies of that k-stage
     int32_t num_groups;
     int32_t prefetch_stages;  // L2 prefetch distance of the producer, in stages (0 = none)
+    float *workspace;         // fp32 partial tiles of split tiles (slots of 128 x BN floats)
+    int *counters;            // per split tile: segments finished so far (0 between launches)
 };
 
 }  // namespace nvfp4

@@ -133,14 +133,31 @@ int nvfp4_last_cuda_error(void);
 
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
+ *  NVFP4_OPT_CTA_PAIR      : 0 = automatic, 1 = CTA pairs, 2 = single CTAs.
+ *                             CTA pairs: each cluster of two CTAs computes 256 x 256
+ *                             output tiles with the pair form of the MMA (M = 256),
+ *                             each SM loading its own 128 A rows and half of the B
+ *                             tile. Automatic (when BLOCK_N and STAGES are 0 too):
+ *                             per problem set, whichever kind finishes its busiest
+ *                             tile list sooner by a measured per-stage cost model
+ *                             (pairs for the MoE-sized sets, single CTAs for small
+ *                             sets that would leave SMs idle). BLOCK_N and STAGES
+ *                             apply to single CTAs only.
  *  NVFP4_OPT_BLOCK_N       : 0 = automatic (128), or 128 or 256: the width of
- *                             the output tiles (and the MMA's N)
+ *                             the single-CTA output tiles (and the MMA's N)
  *  NVFP4_OPT_STAGES        : 0 = automatic (the deepest shared-memory ring that
- *                             fits: 6 stages at BLOCK_N 128, 4 at 256), or 2
+ *                             fits: 6 stages at BLOCK_N 128, 4 at 256, 5 for
+ *                             pairs), or 2 (single CTAs)
  *  NVFP4_OPT_MAX_CTAS      : 0 = one CTA per SM, or an upper bound on the grid
+ *                             (pairs: on twice the number of pairs)
  *  NVFP4_OPT_PREFETCH_STAGES: -1 = automatic (0), or 0..64: how many K-stages
  *                             ahead of its shared-memory ring each CTA prefetches
  *                             its operands into L2
+ *  NVFP4_OPT_SPLIT_TAIL    : 1 = on (default), 0 = off. When all tiles have the same K
+ *                             and do not divide evenly among the CTAs, the last
+ *                             partial wave of tiles is cut along K so that every CTA
+ *                             does the same work (fp32 partials in a library-owned
+ *                             workspace, summed in K order: results are deterministic)
  *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
  *                             (default 2,000,000 us)
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
@@ -155,7 +172,9 @@ enum {
     NVFP4_OPT_MAX_CTAS = 3,
     NVFP4_OPT_WAIT_TIMEOUT_US = 4,
     NVFP4_OPT_FAULT_SKIP_LOAD = 5,
-    NVFP4_OPT_PREFETCH_STAGES = 6
+    NVFP4_OPT_PREFETCH_STAGES = 6,
+    NVFP4_OPT_SPLIT_TAIL = 7,
+    NVFP4_OPT_CTA_PAIR = 8
 };
 int nvfp4_set_option(int option, int64_t value);
 

@@ -1,0 +1,164 @@
+// Host-only check of the tile schedule (no CUDA call is made at run time).
+// Invariants, for several problem sets, tile widths and grid caps:
+//  * every tile's K-stages 0..nk-1 are covered exactly once, by segments in K order;
+//  * a split tile has nseg > 1 segments with seg = 0..nseg-1 and consecutive workspace
+//    slots; a whole tile has split = -1;
+//  * with split_tail on and uniform K, the CTAs' stage counts differ by at most one
+//    plus one tile's worth less than the whole-tile share, i.e. max - min <= nk;
+//  * the list offsets are monotone and end at the item count.
+#include "nvfp4_gemm.cu"
+#include "prepack.cu"
+
+#include <cstdio>
+#include <map>
+#include <tuple>
+
+static int fails = 0;
+#define CHECK(cond, ...)                         \
+    do {                                         \
+        if (!(cond)) {                           \
+            ++fails;                             \
+            std::printf("FAIL %s: ", #cond);     \
+            std::printf(__VA_ARGS__);            \
+            std::printf("\n");                   \
+        }                                        \
+    } while (0)
+
+static void check(const std::vector<ActiveGroup> &gs, int bm, int bn, int cap, bool split)
+{
+    Schedule sc = build_schedule(gs, bm, bn, cap, split);
+    const int lists = sc.grid * kPipes;
+    CHECK((int)sc.list_begin.size() == lists + 1, "lists");
+    CHECK(sc.list_begin[lists] == sc.items.size(), "end");
+    std::map<std::tuple<int, int, int>, std::vector<WorkItem>> by_tile;
+    std::vector<int64_t> load(lists, 0);
+    bool any_split = false;
+    for (int l = 0; l < lists; ++l) {
+        CHECK(sc.list_begin[l] <= sc.list_begin[l + 1], "monotone");
+        bool seen_whole = false;
+        for (uint32_t i = sc.list_begin[l]; i < sc.list_begin[l + 1]; ++i) {
+            const WorkItem &w = sc.items[i];
+            any_split = any_split || w.split >= 0;
+            CHECK(!(seen_whole && w.split >= 0), "split segment after a whole tile in list %d", l);
+            seen_whole = seen_whole || w.split < 0;
+            by_tile[{w.group, w.tile_m, w.tile_n}].push_back(w);
+            load[l] += w.kb_end - w.kb_begin;
+            CHECK(w.kb_end > w.kb_begin, "empty segment");
+        }
+    }
+    size_t tiles = 0;
+    bool uniform = true;
+    int nk0 = -1;
+    for (size_t g = 0; g < gs.size(); ++g) {
+        const int tm = (gs[g].M + bm - 1) / bm, tn = (gs[g].N + bn - 1) / bn, nk = (gs[g].K / 64 + 3) / 4;
+        uniform = uniform && (nk0 < 0 || nk == nk0);
+        nk0 = nk;
+        tiles += (size_t)tm * tn;
+        for (int n = 0; n < tn; ++n)
+            for (int m = 0; m < tm; ++m) {
+                auto it = by_tile.find({(int)g, m, n});
+                CHECK(it != by_tile.end(), "tile missing g=%zu m=%d n=%d", g, m, n);
+                if (it == by_tile.end())
+                    continue;
+                auto segs = it->second;
+                std::sort(segs.begin(), segs.end(), [](const WorkItem &a, const WorkItem &b) { return a.seg < b.seg; });
+                int k = 0;
+                for (size_t j = 0; j < segs.size(); ++j) {
+                    CHECK(segs[j].seg == (int)j && segs[j].nseg == (int)segs.size(), "seg numbering");
+                    CHECK(segs[j].kb_begin == k, "gap or overlap at k=%d", k);
+                    k = segs[j].kb_end;
+                    if (segs.size() > 1)
+                        CHECK(segs[j].split >= 0 && segs[j].ws_slot == segs[0].ws_slot + (int)j &&
+                                  segs[j].split == segs[0].split, "split bookkeeping");
+                    else
+                        CHECK(segs[j].split == -1, "whole tile marked split");
+                }
+                CHECK(k == nk, "K not covered: %d of %d", k, nk);
+            }
+    }
+    CHECK(by_tile.size() == tiles, "extra tiles");
+    CHECK(split || !any_split, "split with split_tail off");
+    const int64_t mx = *std::max_element(load.begin(), load.end()), mn = *std::min_element(load.begin(), load.end());
+    if (any_split) {
+        CHECK(mx - mn <= 1, "imbalance %lld..%lld (bn %d cap %d)", (long long)mn, (long long)mx, bn, cap);
+    } else if (uniform) {
+        // whole tiles dealt round-robin: tile counts differ by at most one
+        CHECK(mx - mn <= nk0, "whole-tile imbalance %lld..%lld", (long long)mn, (long long)mx);
+        // and where splitting was on, it was skipped only when it would save little
+        const int64_t G = sc.grid, unb = (int64_t)((tiles + G - 1) / G) * nk0, bal = ((int64_t)tiles * nk0 + G - 1) / G;
+        if (split && (int64_t)tiles > G && tiles % G != 0)
+            CHECK(unb - bal < 2 || (unb - bal) * 8 < unb, "split skipped though it saves %lld of %lld", (long long)(unb - bal),
+                  (long long)unb);
+    }
+}
+
+static ActiveGroup G(int M, int N, int K) { return ActiveGroup{M, N, K, 0, nullptr, nullptr, nullptr, nullptr, nullptr}; }
+
+int main()
+{
+    std::vector<std::vector<ActiveGroup>> sets = {
+        {G(80, 4096, 7168), G(176, 4096, 7168), G(128, 4096, 7168), G(72, 4096, 7168), G(64, 4096, 7168),
+         G(248, 4096, 7168), G(96, 4096, 7168), G(160, 4096, 7168)},
+        {G(40, 7168, 2048), G(76, 7168, 2048), G(168, 7168, 2048), G(72, 7168, 2048), G(164, 7168, 2048),
+         G(148, 7168, 2048), G(196, 7168, 2048), G(160, 7168, 2048)},
+        {G(192, 3072, 4096), G(320, 3072, 4096)},
+        {G(128, 4096, 1536), G(384, 4096, 1536)},
+        {G(130, 2048, 1024), G(60, 1024, 1024), G(200, 1536, 1024), G(129, 520, 1024)},
+        {G(200, 384, 1536), G(64, 256, 512), G(129, 136, 768)},
+        {G(1, 8, 64)},
+        {G(300, 72, 2304), G(5, 8, 64)},
+    };
+    // single-CTA tiles 128 x 128 and 128 x 256; CTA-pair tiles 256 x 256 (grid = pairs)
+    const int shapes[3][2] = {{128, 128}, {128, 256}, {256, 256}};
+    for (auto &gs : sets)
+        for (auto &sh : shapes)
+            for (int cap : {152, 148, 76, 40, 7, 1})
+                for (bool split : {true, false})
+                    check(gs, sh[0], sh[1], cap, split);
+    // the two MoE sets split at both tile widths, and the K=2048 set at width 128 does not
+    auto splits = [](const std::vector<ActiveGroup> &gs, int bn) {
+        Schedule sc = build_schedule(gs, 128, bn, 152, true);
+        return sc.splits;
+    };
+    CHECK(splits(sets[0], 128) > 0 && splits(sets[0], 256) > 0, "moe K=7168 should split");
+    CHECK(splits(sets[1], 128) == 0 && splits(sets[1], 256) > 0, "moe K=2048 split choice");
+    // the problem set of the GPU split test: splits at grids 70, 72 (width 128) and 36, 37
+    // (width 256), not at 152 or 7
+    const std::vector<ActiveGroup> t4 = {G(130, 2048, 2048), G(60, 1024, 2048), G(200, 1536, 2048), G(129, 520, 2048)};
+    CHECK(build_schedule(t4, 128, 128, 70, true).splits > 0 && build_schedule(t4, 128, 128, 72, true).splits > 0, "t4 128");
+    CHECK(build_schedule(t4, 128, 256, 36, true).splits > 0 && build_schedule(t4, 128, 256, 37, true).splits > 0, "t4 256");
+    CHECK(build_schedule(t4, 128, 128, 152, true).splits == 0 && build_schedule(t4, 128, 256, 7, true).splits == 0, "t4 none");
+    {
+        const Schedule sc = build_schedule(t4, 128, 128, 72, true);
+        int mx = 0;
+        for (const WorkItem &w : sc.items)
+            mx = std::max(mx, w.nseg);
+        CHECK(mx == 8, "t4 at 72 CTAs: one-stage segments, %d per tile", mx);
+    }
+    for (auto cap : {70, 72, 36, 37, 7, 152})
+        for (auto &sh : shapes)
+            check(t4, sh[0], sh[1], cap, true);
+    // the pair kernel's split test set (256 x 256 tiles): 8 + 4 + 6 + 3 = 21 tiles at K = 2048,
+    // so 19 and 20 pairs split the short last wave, 21 and more do not
+    CHECK(build_schedule(t4, 256, 256, 19, true).splits > 0 && build_schedule(t4, 256, 256, 20, true).splits > 0, "pair split");
+    CHECK(build_schedule(t4, 256, 256, 76, true).splits == 0, "pair no split");
+    // the MoE sets on 76 pairs: K=7168 splits (128 tiles), K=2048 splits (224 tiles)
+    CHECK(build_schedule(sets[0], 256, 256, 76, true).splits > 0, "pair moe K=7168");
+    // the automatic choice on a 152-SM device that fits 76 CTA pairs: pairs for the two
+    // MoE-shaped sets, single CTAs for the two-group sets and the tiny one
+    {
+        DeviceState ds;
+        ds.sm_count = 152;
+        ds.pair_clusters = 76;
+        const std::vector<ActiveGroup> g2a = {G(128, 4096, 1536), G(384, 4096, 1536)};
+        const std::vector<ActiveGroup> g2b = {G(192, 3072, 4096), G(320, 3072, 4096)};
+        const std::vector<ActiveGroup> tiny = {G(64, 512, 512), G(128, 512, 512)};
+        CHECK(choose_variant(sets[0], ds, 0, true) == kVariantPair, "moe K=7168 -> pairs");
+        CHECK(choose_variant(sets[1], ds, 0, true) == kVariantPair, "moe K=2048 -> pairs");
+        CHECK(choose_variant(g2a, ds, 0, true) == 0, "g2 K=1536 -> single");
+        CHECK(choose_variant(g2b, ds, 0, true) == 0, "g2 K=4096 -> single");
+        CHECK(choose_variant(tiny, ds, 0, true) == 0, "tiny -> single");
+    }
+    std::printf(fails ? "FAILED %d\n" : "ok\n", fails);
+    return fails ? 1 : 0;
+}

@@ -26,7 +26,8 @@ pytestmark = pytest.mark.gpu
 def _defaults():
     yield
     for opt, val in [(nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_BLOCK_N, 0),
-                     (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000)]:
+                     (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
+                     (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0)]:
         nv.nvfp4_set_option(opt, val)
 
 
@@ -65,12 +66,16 @@ RAGGED = dict(seed=77, Ms=[1, 40, 127, 128, 129, 248, 300], Ns=[8, 120, 136, 512
               Ks=[64, 192, 256, 320, 1024, 512, 2304])
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("layout", [nv.NVFP4_SF_PREPACKED, nv.NVFP4_SF_ROWMAJOR])
-def test_ragged_shapes_one_launch(layout):
+def test_ragged_shapes_one_launch(layout, pair):
+    # CTA pairs: M = 1..300 leaves the second CTA's rows partly or wholly past M, and
+    # N = 8..264 leaves the second half of the B tile partly or wholly past N
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_problem_set(RAGGED["seed"], RAGGED["Ms"], RAGGED["Ns"], RAGGED["Ks"])
     d = [DeviceGroup(g, layout) for g in groups]
     run(d)
-    check_full(groups, d, f"ragged layout={layout}")
+    check_full(groups, d, f"ragged layout={layout} pair={pair}")
 
 
 def test_structured_closed_form():
@@ -179,8 +184,12 @@ def sample_indices(M, N, n, rng):
     return np.array(ms), np.array(ns)
 
 
+@pytest.mark.parametrize("pair", [0, 1, 2])
 @pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
-def test_full_size_workloads_sampled(name):
+def test_full_size_workloads_sampled(name, pair):
+    # pair 0: the automatic choice, the benchmark's launch configuration; 1: CTA pairs;
+    # 2: single CTAs
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_workload(name)
     d = [DeviceGroup(g) for g in groups]
     run(d)  # default options: the launch configuration of the benchmark
@@ -200,3 +209,36 @@ def test_full_size_workloads_sampled(name):
     run(d)
     for f, x in zip(first, d):
         assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
+
+
+# --------------------------------------------------------- split tail tiles ---
+
+@pytest.mark.parametrize("block_n,max_ctas", [(128, 70), (128, 72), (256, 36), (256, 37), (128, 0), (256, 7),
+                                               ("pair", 38), ("pair", 40), ("pair", 0)])
+def test_split_tail_tiles_match_oracle_and_are_deterministic(block_n, max_ctas):
+    # Uniform K (2048 = 8 stages): 74 tiles at width 128, 38 at width 256, 21 pair tiles
+    # of 256 x 256. Grids of 70/72 and 36/37 CTAs, and of 19/20 pairs, leave a short last
+    # wave that is cut along K (down to one-stage segments, eight per tile, at 72 and 37
+    # CTAs); the full grid and 7 CTAs do not split.
+    groups = gen.make_problem_set(41, [130, 60, 200, 129], [2048, 1024, 1536, 520], [2048] * 4)
+    if block_n == "pair":
+        nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 1)
+    else:
+        nv.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, block_n)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, max_ctas)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    check_full(groups, d, f"split block_n={block_n} max_ctas={max_ctas}")
+    first = [x.result().copy() for x in d]
+    for x in d:
+        x.reset()
+    run(d)  # same schedule again: the same bits (partials are summed in K order)
+    for f, x in zip(first, d):
+        assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
+    nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 0)
+    try:
+        e = [DeviceGroup(g) for g in groups]
+        run(e)
+        check_full(groups, e, "split off")
+    finally:
+        nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 1)

@@ -28,10 +28,12 @@ pytestmark = pytest.mark.gpu
 CASES = [([128], [128], [4096]), ([64, 128], [512, 512], [512, 512])]
 
 
+@pytest.mark.parametrize("pair", [1, 2])
 @pytest.mark.parametrize("Ms,Ns,Ks", CASES)
-def test_wait_timeout_reports_and_recovers(Ms, Ns, Ks):
+def test_wait_timeout_reports_and_recovers(Ms, Ns, Ks, pair):
     groups = gen.make_problem_set(1, Ms, Ns, Ks)
     d = [DeviceGroup(g) for g in groups]
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     try:
         nv.nvfp4_set_option(nv.NVFP4_OPT_WAIT_TIMEOUT_US, 20000)
         nv.nvfp4_set_option(nv.NVFP4_OPT_FAULT_SKIP_LOAD, 0)
@@ -43,10 +45,13 @@ def test_wait_timeout_reports_and_recovers(Ms, Ns, Ks):
     finally:
         nv.nvfp4_set_option(nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1)
         nv.nvfp4_set_option(nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000)
-    for x in d:
-        x.reset()
-    nv.nvfp4_grouped_gemm([x.problem() for x in d])
-    torch.cuda.synchronize()
-    assert nv.nvfp4_device_status()[0] == 0
-    for g, x, (c, s) in zip(groups, d, oracle.grouped_gemm(groups)):
-        assert_within_bound(x.result(), c, s, "after recovery")
+    try:
+        for x in d:
+            x.reset()
+        nv.nvfp4_grouped_gemm([x.problem() for x in d])
+        torch.cuda.synchronize()
+        assert nv.nvfp4_device_status()[0] == 0
+        for g, x, (c, s) in zip(groups, d, oracle.grouped_gemm(groups)):
+            assert_within_bound(x.result(), c, s, "after recovery")
+    finally:
+        nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 0)
