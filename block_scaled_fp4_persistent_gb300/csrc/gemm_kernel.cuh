@@ -64,6 +64,9 @@ constexpr uint32_t kTmemCols = 512;
 // Roles reported in the status words.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleTeardown = 3, kRoleScales = 4;
 
+// Named barriers: 0 is __syncthreads, 1 the epilogue warps', 2 the start-up one.
+constexpr uint32_t kEpilogueBarrier = 1, kSetupBarrier = 2;
+
 template <int BN, int STAGES>
 struct Layout {
     static constexpr int kHalves = BN / 128;                       // 128-row halves of the B tile
@@ -183,8 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     const int warp = threadIdx.x / 32;
     const uint32_t lane = threadIdx.x % 32;
     const Table *tab = args.table;
-    const uint32_t item_begin = tab->cta_begin(blockIdx.x);
-    const uint32_t item_end = tab->cta_begin(blockIdx.x + 1);
+    const uint32_t item_begin = args.list_begin[blockIdx.x];
+    const uint32_t item_end = args.list_begin[blockIdx.x + 1];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -198,14 +201,22 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         sh->abort = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
-        tmem_alloc(smem_addr(tmem_base_word), kTmemCols);
-        tmem_relinquish();
+    // The producer needs nothing but the barriers its lane 0 just initialised, so
+    // it starts at once; the other warps also wait for the TMEM allocation.
+    uint32_t tmem_base = 0;
+    if (warp == kProducerWarp) {
+        __syncwarp();
+        named_barrier_arrive(kSetupBarrier, kThreads);
+    } else {
+        if (warp == kMmaWarp) {
+            tmem_alloc(smem_addr(tmem_base_word), kTmemCols);
+            tmem_relinquish();
+        }
+        tc_fence_before();
+        named_barrier_sync(kSetupBarrier, kThreads);
+        tc_fence_after();
+        tmem_base = *tmem_base_word;
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_base_word;
     const uint32_t tmem_sf = tmem_base + L::kSfCol0;
 
     if (warp == kProducerWarp) {
@@ -230,28 +241,26 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 const uint8_t *sfa;
                 const uint8_t *sfb[L::kHalves];
             };
+            // Everything but the tensor maps' addresses comes from the item itself.
             auto source = [&](uint32_t it) {
                 Src r;
                 const WorkItem w = tab->item(it);
-                const GroupEntry &ge = tab->group(w.group);
+                const GroupEntry &ge = tab->group(w.group);  // address only: no load
                 r.tmap_a = &ge.tmap_a;
                 r.tmap_b = &ge.tmap_b;
                 r.ya = w.tile_m * kBlockM;
                 r.yb = w.tile_n * BN;
-                r.kb64 = ge.kblocks64;
+                r.kb64 = w.kblocks64;
                 r.kb_begin = w.kb_begin;
                 r.kb_end = w.kb_end;
-                r.b_shared = ge.tiles_m > 1;
-                r.sfa = ge.sfa + (size_t)w.tile_m * r.kb64 * kScaleBlockBytes;
+                r.b_shared = (w.flags & kItemBShared) != 0;
+                r.sfa = w.sfa;
                 // The scales of B come in 128-row tiles. A half of the B tile that lies
                 // wholly past N reads the first half's scales instead: its B rows are
                 // zero (TMA fills them), so the scales only need to be finite.
-                const int rt_b = (ge.N + 127) / 128;
-#pragma unroll
-                for (int h = 0; h < L::kHalves; ++h) {
-                    const int rt = w.tile_n * L::kHalves + h;
-                    r.sfb[h] = ge.sfb + (size_t)(rt < rt_b ? rt : w.tile_n * L::kHalves) * r.kb64 * kScaleBlockBytes;
-                }
+                r.sfb[0] = w.sfb;
+                if (L::kHalves > 1)
+                    r.sfb[L::kHalves - 1] = w.sfb + ((w.flags & kItemB2) ? (size_t)r.kb64 * kScaleBlockBytes : 0);
                 return r;
             };
             // prefetch cursor
@@ -337,7 +346,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = tab->item(it);
-                const int kb64 = tab->group(w.group).kblocks64;
+                const int kb64 = w.kblocks64;
                 // the epilogue warps must have drained the previous tile's accumulator
                 if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
                     ok = false;
@@ -513,10 +522,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 // Count this segment in. The segment that completes the count sums all of
                 // them; nothing ever waits for another CTA.
                 __threadfence();
-                named_barrier_sync(1, kEpilogueWarps * 32);
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
                 if (e == 0)
                     sh->last = (atomicAdd(&args.counters[w.split], 1) == w.nseg - 1) ? 1 : 0;
-                named_barrier_sync(1, kEpilogueWarps * 32);
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
                 if (sh->last) {
                     __threadfence();
                     const float4 *ws0 = reinterpret_cast<const float4 *>(args.workspace +
@@ -555,7 +564,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     if (e == 0)
                         args.counters[w.split] = 0;  // ready for the next launch
                 }
-                named_barrier_sync(1, kEpilogueWarps * 32);  // sh->last is read before it is rewritten
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);  // sh->last is read before it is rewritten
             }
         }
     }

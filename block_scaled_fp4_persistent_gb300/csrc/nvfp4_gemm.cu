@@ -93,6 +93,7 @@ struct CachedTable {
     int grid = 0;
     int block_n = 0;
     int variant = 0;  // the kernel variant the table was built for
+    std::vector<uint32_t> list_begin;  // the table's cta_begin, passed again with each launch
 };
 std::list<CachedTable> g_tables;  // most recently used first
 std::unordered_map<uint64_t, std::list<CachedTable>::iterator> g_table_index;
@@ -243,6 +244,35 @@ struct ActiveGroup {
 // once and from L2 after that. Each SM's two pipelines take alternate waves.
 inline int list_of_tile(size_t t, int grid) { return (int)(t % grid) * kPipes + (int)((t / grid) % kPipes); }
 
+// A work item with the producer's fields filled in (see WorkItem): the scale
+// blocks of the tile's first 128-row tiles of A and B, and whether the second
+// 128-row halves (of a 256-row A tile, of a 256-wide B tile) hold any rows.
+WorkItem make_item(const ActiveGroup &g, int group, int m, int n, int kb_begin, int kb_end, int split, int seg,
+                   int nseg, int slot, int block_m, int block_n)
+{
+    WorkItem w{};
+    w.group = group;
+    w.tile_m = m;
+    w.tile_n = n;
+    w.kb_begin = kb_begin;
+    w.kb_end = kb_end;
+    w.split = split;
+    w.seg = seg;
+    w.nseg = nseg;
+    w.ws_slot = slot;
+    const int kb64 = g.K / 64;
+    w.kblocks64 = kb64;
+    const int row_tiles_a = (g.M + 127) / 128, row_tiles_b = (g.N + 127) / 128;
+    const int ra = m * (block_m / 128), rb = n * (block_n / 128);
+    w.flags = ((g.M + block_m - 1) / block_m > 1 ? kItemBShared : 0) |
+              (block_m == 256 && ra + 1 < row_tiles_a ? kItemA2 : 0) |
+              (block_n == 256 && rb + 1 < row_tiles_b ? kItemB2 : 0);
+    const size_t blocks = (size_t)kb64 * kScaleBlockBytes;
+    w.sfa = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFA) + (size_t)ra * blocks);
+    w.sfb = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFB) + (size_t)rb * blocks);
+    return w;
+}
+
 struct Schedule {
     std::vector<WorkItem> items;
     std::vector<uint32_t> list_begin;
@@ -298,7 +328,7 @@ Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int blo
     std::vector<std::vector<WorkItem>> head(lists), per(lists);
     for (size_t t = 0; t < whole; ++t) {
         const Tile &x = tiles[t];
-        per[list_of_tile(t, G)].push_back(WorkItem{x.group, x.m, x.n, 0, x.nk, -1, 0, 1, 0, {0, 0, 0}});
+        per[list_of_tile(t, G)].push_back(make_item(gs[x.group], x.group, x.m, x.n, 0, x.nk, -1, 0, 1, 0, block_m, block_n));
     }
     if (whole < T) {
         const int nk = tiles[0].nk;
@@ -324,7 +354,8 @@ Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int blo
             for (int j = 0; j < nseg; ++j) {
                 const int slot = nseg > 1 ? sc.ws_slots++ : 0;
                 head[segs[j].first * kPipes].push_back(
-                    WorkItem{x.group, x.m, x.n, segs[j].second.first, segs[j].second.second, split, j, nseg, slot, {0, 0, 0}});
+                    make_item(gs[x.group], x.group, x.m, x.n, segs[j].second.first, segs[j].second.second, split, j, nseg,
+                              slot, block_m, block_n));
             }
         }
     }
@@ -352,7 +383,7 @@ Plan plan_for(int variant, const DeviceState &ds, int64_t max_ctas)
     p.variant = variant;
     p.block_m = pair ? kPairBlockM : kBlockM;
     p.block_n = pair ? kPairBlockN : (variant >= 2 ? 256 : 128);
-    int cap = pair ? ds.pair_clusters : ds.sm_count;
+    int cap = std::min(pair ? ds.pair_clusters : ds.sm_count, kMaxLists);
     if (max_ctas > 0)
         cap = (int)std::min<int64_t>(pair ? std::max<int64_t>(1, max_ctas / 2) : max_ctas, cap);
     p.grid_cap = cap;
@@ -429,6 +460,7 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     t.grid = grid * halves;
     t.block_n = block_n;
     t.variant = variant;
+    t.list_begin = sc.list_begin;
     CUDA_TRY(cudaMallocHost(&t.host, total));
     memset(t.host, 0, total);
     uint8_t *h = static_cast<uint8_t *>(t.host);
@@ -542,6 +574,7 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
                                                                        : g_opt.prefetch_stages.load());
     args.workspace = t.workspace;
     args.counters = t.counters;
+    std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;
@@ -583,6 +616,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.prefetch_stages = 0;
     args.workspace = t.workspace;
     args.counters = t.counters;
+    std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     nvfp4_pair_gemm_kernel<kPairStages><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;
@@ -985,7 +1019,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         return rc;
     const int cap = g_opt.max_ctas.load() > 0 ? (int)std::min<int64_t>(g_opt.max_ctas.load(), nd->sm_count)
                                               : nd->sm_count;
-    const int grid = (int)std::max<size_t>(1, std::min<size_t>(ntiles, (size_t)cap));
+    const int grid = (int)std::max<size_t>(1, std::min<size_t>(ntiles, (size_t)std::min(cap, kMaxLists)));
     const size_t off_groups = sizeof(TableHeader);
     const size_t off_cta = off_groups + ngroups * sizeof(GroupEntry);
     const int lists = grid * kPipes;
@@ -1052,10 +1086,11 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         e.kblocks64 = p.K / 64;
         e.tiles_m = (p.M + kBlockM - 1) / kBlockM;
         e.tiles_n = (p.N + BN - 1) / BN;
+        const ActiveGroup a{p.M, p.N, p.K, 0, p.A, p.B, p.SFA, p.SFB, p.C};
         for (int n = 0; n < e.tiles_n; ++n)
             for (int m = 0; m < e.tiles_m; ++m, ++t)
                 items[cta_begin[list_of_tile(t, grid)] + t / ((size_t)kPipes * grid)] =
-                    WorkItem{gi, m, n, 0, (p.K / 64 + 3) / 4, -1, 0, 1, 0, {0, 0, 0}};
+                    make_item(a, gi, m, n, 0, (p.K / 64 + 3) / 4, -1, 0, 1, 0, kBlockM, BN);
         ++gi;
     }
 
@@ -1076,6 +1111,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.prefetch_stages = kDefaultPrefetchStages;
     args.workspace = nullptr;  // no split tiles here
     args.counters = nullptr;
+    std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
     nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     return NVFP4_OK;

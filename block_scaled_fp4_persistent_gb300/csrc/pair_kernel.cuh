@@ -94,8 +94,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t rank = cluster_rank();
     const Table *tab = args.table;
     const int pair = blockIdx.x >> 1;
-    const uint32_t item_begin = tab->cta_begin(pair);
-    const uint32_t item_end = tab->cta_begin(pair + 1);
+    const uint32_t item_begin = args.list_begin[pair];
+    const uint32_t item_end = args.list_begin[pair + 1];
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -109,15 +109,27 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         sh->abort = 0;
         fence_barrier_init();
     }
-    if (warp == kMmaWarp) {
-        tmem_alloc_pair(smem_addr(tmem_base_word), kTmemCols);
-        tmem_relinquish_pair();
+    // The producer needs nothing but the barriers its lane 0 just initialised, so
+    // it starts at once (it sends nothing to the peer). The other warps also wait
+    // for the TMEM allocation and for the peer's barriers to exist, since the
+    // leader's commits and the peer's arrivals cross the pair.
+    uint32_t tmem_base = 0;
+    if (warp == kProducerWarp) {
+        __syncwarp();
+        named_barrier_arrive(kSetupBarrier, kThreads);
+        cluster_arrive();
+    } else {
+        if (warp == kMmaWarp) {
+            tmem_alloc_pair(smem_addr(tmem_base_word), kTmemCols);
+            tmem_relinquish_pair();
+        }
+        tc_fence_before();
+        named_barrier_sync(kSetupBarrier, kThreads);
+        cluster_arrive();
+        cluster_wait();
+        tc_fence_after();
+        tmem_base = *tmem_base_word;
     }
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // both CTAs' barriers exist before any arrival from the peer
-    tc_fence_after();
-    const uint32_t tmem_base = *tmem_base_word;
     const uint32_t tmem_sf = tmem_base + L::kSfCol0;
 
     if (warp == kProducerWarp) {
@@ -134,24 +146,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = tab->item(it);
-                const GroupEntry &ge = tab->group(w.group);
-                const int kb64 = ge.kblocks64;
+                const GroupEntry &ge = tab->group(w.group);  // address only: the tensor maps
+                const int kb64 = w.kblocks64;
                 const int32_t ya = w.tile_m * kPairBlockM + (int)rank * 128;
                 const int32_t yb = w.tile_n * kPairBlockN + (int)rank * 128;
                 // Scale blocks come in 128-row tiles. A 128-row half that lies wholly
                 // past M (or N) reads the tile's first half's scales instead: its
                 // operand rows are zero (TMA fills them), so the scales need only be
                 // finite.
-                const int rt_a_all = (ge.M + 127) / 128, rt_b_all = (ge.N + 127) / 128;
-                const int rta = w.tile_m * 2 + (int)rank;
-                const uint8_t *sfa = ge.sfa + (size_t)(rta < rt_a_all ? rta : w.tile_m * 2) * kb64 * kScaleBlockBytes;
-                const uint8_t *sfb[2];
-#pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int rt = w.tile_n * 2 + h;
-                    sfb[h] = ge.sfb + (size_t)(rt < rt_b_all ? rt : w.tile_n * 2) * kb64 * kScaleBlockBytes;
-                }
-                const uint64_t pol_b = ge.tiles_m > 1 ? pol_b_shared : pol_b_stream;
+                const size_t half = (size_t)kb64 * kScaleBlockBytes;
+                const uint8_t *sfa = w.sfa + ((rank == 1 && (w.flags & kItemA2)) ? half : 0);
+                const uint8_t *sfb[2] = {w.sfb, w.sfb + ((w.flags & kItemB2) ? half : 0)};
+                const uint64_t pol_b = (w.flags & kItemBShared) ? pol_b_shared : pol_b_stream;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++kiter) {
                     if (!wait_phase(smem_addr(&empty[stage]), phase ^ 1u, sh, args, kRoleProducer, (int)it, kb)) {
                         ok = false;
@@ -199,7 +205,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = tab->item(it);
-                const int kb64 = tab->group(w.group).kblocks64;
+                const int kb64 = w.kblocks64;
                 if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
                     ok = false;
                     break;
@@ -396,10 +402,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 if (lane == 0)
                     release_accumulator();
                 __threadfence();
-                named_barrier_sync(1, kEpilogueWarps * 32);
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
                 if (e == 0)
                     sh->last = (atomicAdd(&args.counters[2 * w.split + (int)rank], 1) == w.nseg - 1) ? 1 : 0;
-                named_barrier_sync(1, kEpilogueWarps * 32);
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
                 if (sh->last) {
                     __threadfence();
                     // this half's slot of segment sg is 2 * (ws_slot - seg + sg) + rank
@@ -437,7 +443,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (e == 0)
                         args.counters[2 * w.split + (int)rank] = 0;  // ready for the next launch
                 }
-                named_barrier_sync(1, kEpilogueWarps * 32);
+                named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
             }
         }
         // every store of C must be complete before the CTA exits
@@ -446,6 +452,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         __syncwarp();
     }
 
+    if (warp == kProducerWarp)
+        cluster_wait();  // the producer's part of the start-up cluster barrier
     tc_fence_before();
     __syncthreads();
     cluster_sync();  // no arrival from the peer after this point

@@ -32,6 +32,13 @@ __device__ __forceinline__ void named_barrier_sync(uint32_t id, uint32_t threads
     asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Arrives on named barrier `id` without waiting (the threads that wait use
+// named_barrier_sync with the same count).
+__device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t threads)
+{
+    asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
+}
+
 // ----------------------------------------------------------------- cluster --
 
 // Rank of this CTA in its cluster (0 or 1 for a CTA pair).
@@ -48,6 +55,10 @@ __device__ __forceinline__ void cluster_sync()
 {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
+
+// The two halves of cluster_sync, for a warp that arrives early and waits later.
+__device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
+__device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
 
 // The shared::cluster address of the object at shared::cta address `addr` in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank)

@@ -36,6 +36,12 @@ struct alignas(128) GroupEntry {
 // its fp32 partial to workspace slot ws_slot, and the one that finishes last
 // (counted in counters[split]) sums the slots ws_slot - seg .. ws_slot - seg +
 // nseg - 1 in that order and stores C.
+//
+// The item also carries what the TMA producer needs before its first copy, so
+// that copy waits for one load (the item) rather than a chain of them:
+// kblocks64 = K / 64, the scale blocks of the tile's first 128-row tiles of A
+// and B, and flags telling whether the second 128-row half of the A tile (CTA
+// pairs) and of the B tile (256-wide tiles) holds any rows.
 struct WorkItem {
     int32_t group;
     int32_t tile_m;
@@ -46,10 +52,18 @@ struct WorkItem {
     int32_t seg;
     int32_t nseg;
     int32_t ws_slot;
-    int32_t reserved[3];
+    int32_t kblocks64;
+    int32_t flags;  // kItemBShared | kItemA2 | kItemB2
+    int32_t reserved;
+    const uint8_t *sfa;  // scale blocks of the tile's first 128 A rows (kblocks64 blocks of 512 B)
+    const uint8_t *sfb;  // scale blocks of the tile's first 128 B rows
 };
 
-static_assert(sizeof(WorkItem) == 48, "WorkItem is read as three int4");
+constexpr int32_t kItemBShared = 1;  // the group has several m-tiles: its B tiles are read more than once
+constexpr int32_t kItemA2 = 2;       // rows 128..255 of the tile's A rows exist (their scales follow sfa)
+constexpr int32_t kItemB2 = 4;       // rows 128..255 of the tile's B rows exist (their scales follow sfb)
+
+static_assert(sizeof(WorkItem) == 64, "WorkItem is read as four int4");
 
 struct alignas(128) TableHeader {
     int32_t num_groups;
@@ -73,15 +87,27 @@ struct Table {
     }
     __host__ __device__ WorkItem item(uint32_t i) const
     {
-        const int4 *p = reinterpret_cast<const int4 *>(reinterpret_cast<const char *>(this) + h.off_items) + 3 * i;
-        const int4 a = p[0], b = p[1], c = p[2];
-        return WorkItem{a.x, a.y, a.z, a.w, b.x, b.y, b.z, b.w, c.x, {0, 0, 0}};
+        const int4 *p = reinterpret_cast<const int4 *>(reinterpret_cast<const char *>(this) + h.off_items) + 4 * i;
+        const int4 a = p[0], b = p[1], c = p[2], d = p[3];
+        WorkItem w;
+        w.group = a.x, w.tile_m = a.y, w.tile_n = a.z, w.kb_begin = a.w;
+        w.kb_end = b.x, w.split = b.y, w.seg = b.z, w.nseg = b.w;
+        w.ws_slot = c.x, w.kblocks64 = c.y, w.flags = c.z, w.reserved = c.w;
+        w.sfa = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.x | ((uint64_t)(uint32_t)d.y << 32));
+        w.sfb = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.z | ((uint64_t)(uint32_t)d.w << 32));
+        return w;
     }
     int num_groups_host() const { return h.num_groups; }
 };
 
+// Tile lists per launch: one per CTA, or per CTA pair.
+constexpr int kMaxLists = 256;
+
 struct KernelArgs {
     const Table *table;
+    // List l holds items list_begin[l] .. list_begin[l+1]-1. A copy of the table's
+    // cta_begin array, passed with the launch so that no CTA waits for it.
+    uint32_t list_begin[kMaxLists + 1];
     int *status;            // 4 words: code, role, item, stage
     uint64_t timeout_ns;    // bound of every wait
     int32_t fault_skip_load;  // -1 off; else CTA 0 skips the copies of that k-stage
