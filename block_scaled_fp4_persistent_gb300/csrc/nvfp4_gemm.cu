@@ -47,7 +47,7 @@ struct Options {
     std::atomic<int64_t> timeout_us{2000000};
     std::atomic<int64_t> fault_skip_load{-1};
     std::atomic<int64_t> prefetch_stages{-1};  // -1 = automatic
-    std::atomic<int64_t> split_tail{1};
+    std::atomic<int64_t> split_tail{1};  // 0 off, 1 single CTAs only, 2 single CTAs and pairs
     std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
 } g_opt;
 
@@ -390,39 +390,55 @@ Plan plan_for(int variant, const DeviceState &ds, int64_t max_ctas)
     return p;
 }
 
-// K-stages of the busiest list.
-int64_t makespan_stages(const Schedule &sc)
+// Whether a variant's schedule cuts its last partial wave along K. On the pair
+// kernel the fp32 partials of 256 x 256 tiles (their write, the reduction's
+// reads) cost more than the balance gains: on the MoE-shaped set with K = 7168
+// it measured 40.5 us split against 38.0 us whole. So pairs split only when
+// asked to (split_mode 2).
+bool split_for(int variant, int split_mode)
 {
-    int64_t worst = 0;
+    return split_mode == 2 || (split_mode == 1 && variant != kVariantPair);
+}
+
+// Estimated time of a schedule's busiest list, in microseconds: stage_us per
+// K-stage, plus 1 us per item (the tile change: accumulator drain, epilogue,
+// refilling the ring) and 1 us more per split segment (its fp32 partial).
+double makespan_us(const Schedule &sc, double stage_us)
+{
+    double worst = 0;
     for (size_t l = 0; l + 1 < sc.list_begin.size(); ++l) {
-        int64_t sum = 0;
+        double t = 0;
         for (uint32_t i = sc.list_begin[l]; i < sc.list_begin[l + 1]; ++i)
-            sum += sc.items[i].kb_end - sc.items[i].kb_begin;
-        worst = std::max(worst, sum);
+            t += stage_us * (sc.items[i].kb_end - sc.items[i].kb_begin) + (sc.items[i].split >= 0 ? 2.0 : 1.0);
+        worst = std::max(worst, t);
     }
     return worst;
 }
 
 // The automatic choice between CTA pairs and single CTAs with 128 x 128 tiles,
-// from each schedule's busiest list. Measured on this GPU: a K-stage takes about
-// 0.35 us on a single CTA (128 x 128 outputs) and 0.40 us on a CTA pair
-// (256 x 256), and a pair reaches its first MMA about 1 us later. So pairs win
-// where they cut the busiest list's stages by more than ~15% plus that microsecond:
-// the MoE-sized problem sets; small ones that leave SMs idle stay on single CTAs.
-int choose_variant(const std::vector<ActiveGroup> &gs, const DeviceState &ds, int64_t max_ctas, bool split_tail)
+// from each schedule's busiest list. Measured on this GPU with every SM busy: a
+// K-stage takes about 0.39 us on a single CTA (128 x 128 outputs) and 0.44 us on
+// a CTA pair (256 x 256 outputs), and a pair reaches its first MMA about 1 us
+// later. The MoE-shaped sets go to pairs (K = 7168: 38 us against 41.6 us; K =
+// 2048: 25.4 against 31.9); the two-group sets, which leave SMs idle either way,
+// stay on single CTAs (16.6 against about 18; 12.3 against about 14).
+int choose_variant(const std::vector<ActiveGroup> &gs, const DeviceState &ds, int64_t max_ctas, int split_mode)
 {
     const Plan pp = plan_for(kVariantPair, ds, max_ctas), p1 = plan_for(0, ds, max_ctas);
-    const double t_pair = 1.0 + 0.40 * (double)makespan_stages(build_schedule(gs, pp.block_m, pp.block_n, pp.grid_cap, split_tail));
-    const double t_single = 0.35 * (double)makespan_stages(build_schedule(gs, p1.block_m, p1.block_n, p1.grid_cap, split_tail));
+    const double t_pair = 1.0 + makespan_us(build_schedule(gs, pp.block_m, pp.block_n, pp.grid_cap,
+                                                           split_for(kVariantPair, split_mode)),
+                                            0.44);
+    const double t_single =
+        makespan_us(build_schedule(gs, p1.block_m, p1.block_n, p1.grid_cap, split_for(0, split_mode)), 0.39);
     return t_pair < t_single ? kVariantPair : 0;
 }
 
 // Caller holds g_mu. variant_req is a kernel variant or kVariantAuto.
 int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs, int variant_req, int64_t max_ctas,
-              bool split_tail, cudaStream_t stream, CachedTable **out)
+              int split_mode, cudaStream_t stream, CachedTable **out)
 {
     std::vector<uint8_t> sig(sizeof(int) * 5 + gs.size() * sizeof(ActiveGroup));
-    int hdr[5] = {dev, variant_req, (int)std::min<int64_t>(max_ctas, 1 << 30), 0, split_tail ? 1 : 0};
+    int hdr[5] = {dev, variant_req, (int)std::min<int64_t>(max_ctas, 1 << 30), 0, split_mode};
     memcpy(sig.data(), hdr, sizeof(hdr));
     if (!gs.empty())
         memcpy(sig.data() + sizeof(hdr), gs.data(), gs.size() * sizeof(ActiveGroup));
@@ -437,12 +453,12 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         return rc;
 
     // The pair kernel (variant kVariantPair) runs 256 x 256 tiles, one list per CTA pair.
-    const int variant = variant_req == kVariantAuto ? choose_variant(gs, ds, max_ctas, split_tail) : variant_req;
+    const int variant = variant_req == kVariantAuto ? choose_variant(gs, ds, max_ctas, split_mode) : variant_req;
     const Plan plan = plan_for(variant, ds, max_ctas);
     const bool pair = variant == kVariantPair;
     const int block_m = plan.block_m, block_n = plan.block_n;
     const int halves = pair ? 2 : 1;  // workspace slots and counters per split segment / tile
-    Schedule sc = build_schedule(gs, block_m, block_n, plan.grid_cap, split_tail);
+    Schedule sc = build_schedule(gs, block_m, block_n, plan.grid_cap, split_for(variant, split_mode));
     const std::vector<WorkItem> &items = sc.items;
     const std::vector<uint32_t> &cta_begin = sc.list_begin;
     const int grid = sc.grid;  // lists: CTAs, or CTA pairs
@@ -724,7 +740,7 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         if (int rc = prepare_pair_kernel(*ds))  // also learns how many CTA pairs fit at once
             return rc;
     CachedTable *t = nullptr;
-    if (int rc2 = get_table(dev, *ds, gs, variant_req, g_opt.max_ctas.load(), g_opt.split_tail.load() != 0, stream, &t))
+    if (int rc2 = get_table(dev, *ds, gs, variant_req, g_opt.max_ctas.load(), (int)g_opt.split_tail.load(), stream, &t))
         return rc2;
     const int variant = t->variant;
     int rc = NVFP4_OK;
@@ -845,7 +861,7 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         g_opt.timeout_us = value;
         return NVFP4_OK;
     case NVFP4_OPT_SPLIT_TAIL:
-        if (value != 0 && value != 1)
+        if (value < 0 || value > 2)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.split_tail = value;
         return NVFP4_OK;

@@ -153,11 +153,14 @@ int nvfp4_last_cuda_error(void);
  *  NVFP4_OPT_PREFETCH_STAGES: -1 = automatic (0), or 0..64: how many K-stages
  *                             ahead of its shared-memory ring each CTA prefetches
  *                             its operands into L2
- *  NVFP4_OPT_SPLIT_TAIL    : 1 = on (default), 0 = off. When all tiles have the same K
+ *  NVFP4_OPT_SPLIT_TAIL    : 1 = single CTAs only (default), 2 = single CTAs and
+ *                             CTA pairs, 0 = off. When all tiles have the same K
  *                             and do not divide evenly among the CTAs, the last
  *                             partial wave of tiles is cut along K so that every CTA
  *                             does the same work (fp32 partials in a library-owned
- *                             workspace, summed in K order: results are deterministic)
+ *                             workspace, summed in K order: results are deterministic).
+ *                             It is applied only where it saves at least an eighth of
+ *                             the busiest CTA's work.
  *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
  *                             (default 2,000,000 us)
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of

@@ -153,11 +153,11 @@ int main()
         const std::vector<ActiveGroup> g2a = {G(128, 4096, 1536), G(384, 4096, 1536)};
         const std::vector<ActiveGroup> g2b = {G(192, 3072, 4096), G(320, 3072, 4096)};
         const std::vector<ActiveGroup> tiny = {G(64, 512, 512), G(128, 512, 512)};
-        CHECK(choose_variant(sets[0], ds, 0, true) == kVariantPair, "moe K=7168 -> pairs");
-        CHECK(choose_variant(sets[1], ds, 0, true) == kVariantPair, "moe K=2048 -> pairs");
-        CHECK(choose_variant(g2a, ds, 0, true) == 0, "g2 K=1536 -> single");
-        CHECK(choose_variant(g2b, ds, 0, true) == 0, "g2 K=4096 -> single");
-        CHECK(choose_variant(tiny, ds, 0, true) == 0, "tiny -> single");
+        CHECK(choose_variant(sets[0], ds, 0, 1) == kVariantPair, "moe K=7168 -> pairs");
+        CHECK(choose_variant(sets[1], ds, 0, 1) == kVariantPair, "moe K=2048 -> pairs");
+        CHECK(choose_variant(g2a, ds, 0, 1) == 0, "g2 K=1536 -> single");
+        CHECK(choose_variant(g2b, ds, 0, 1) == 0, "g2 K=4096 -> single");
+        CHECK(choose_variant(tiny, ds, 0, 1) == 0, "tiny -> single");
     }
     std::printf(fails ? "FAILED %d\n" : "ok\n", fails);
     return fails ? 1 : 0;

@@ -223,6 +223,7 @@ def test_split_tail_tiles_match_oracle_and_are_deterministic(block_n, max_ctas):
     groups = gen.make_problem_set(41, [130, 60, 200, 129], [2048, 1024, 1536, 520], [2048] * 4)
     if block_n == "pair":
         nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 1)
+        nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 2)  # pairs split only when asked to
     else:
         nv.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, block_n)
     nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, max_ctas)
