@@ -54,8 +54,8 @@ import gen  # noqa: E402
 NOMINAL_BF16_TFLOPS = 2250.0
 NOMINAL_FP4_TFLOPS = 13500.0  # dense NVFP4, GB300
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
-GEMM_KERNEL_NAME = "nvfp4_grouped_gemm_kernel"
 KERNEL_SOURCES = ["block_scaled_fp4_persistent_gb300/csrc/gemm_kernel.cuh",
+                  "block_scaled_fp4_persistent_gb300/csrc/pair_kernel.cuh",
                   "block_scaled_fp4_persistent_gb300/csrc/ptx.cuh",
                   "block_scaled_fp4_persistent_gb300/csrc/table.h"]
 
@@ -93,10 +93,11 @@ def kernel_source_hash():
     return h.hexdigest()[:16]
 
 
-def profiled_traffic(workload):
+def profiled_traffic(kernel, workload):
     """dram read+write bytes per launch from the committed ncu summary of this
-    workload, or None when that summary was taken on other kernel sources."""
-    path = os.path.join(ROOT, "profiles", f"{GEMM_KERNEL_NAME}_{workload}.txt")
+    kernel on this workload, or None when that summary was taken on other kernel
+    sources."""
+    path = os.path.join(ROOT, "profiles", f"{kernel.split('<')[0]}_{workload}.txt")
     if not os.path.exists(path):
         return None
     fields = {}
@@ -277,6 +278,7 @@ def run_ours(args, groups, rank, world, local_rank):
         flush()
         nv.nvfp4_grouped_gemm(probs, stream)
     torch.cuda.synchronize()
+    kernel = nv.nvfp4_last_kernel()
     st, detail = nv.nvfp4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
@@ -387,8 +389,8 @@ def run_ours(args, groups, rank, world, local_rank):
                               "fp4_peak_kind": f"{peak_kind} bf16 x nominal fp4/bf16 ratio 6"},
         "roofline": {"bound": "hbm", "achieved": round(achieved_gbs, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} (copy bandwidth)",
-                     "algorithmic_bytes_per_launch": nbytes, "traffic": profiled_traffic(args.workload),
-                     "kernel": GEMM_KERNEL_NAME},
+                     "algorithmic_bytes_per_launch": nbytes, "traffic": profiled_traffic(kernel, args.workload),
+                     "kernel": kernel},
         "gpu_launches": args.steps,
         "time_share": {"gemm": round(sum(per_call_ms) / (sum(per_call_ms) + sum(flush_ms)), 4),
                        "l2_flush": round(sum(flush_ms) / (sum(per_call_ms) + sum(flush_ms)), 4)},

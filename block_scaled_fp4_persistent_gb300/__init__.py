@@ -10,7 +10,7 @@ been built, the first call raises ImportError. Build it with
 
 Names match the C ABI: ``nvfp4_grouped_gemm``, ``nvfp4_prepack_scales``,
 ``nvfp4_prepacked_scale_bytes``, ``nvfp4_device_status``,
-``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_set_option`` and
+``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_last_kernel``, ``nvfp4_set_option`` and
 ``nvfp4_release``.
 """
 from __future__ import annotations
@@ -80,6 +80,8 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_status_string.argtypes = [ctypes.c_int]
     lib.nvfp4_last_cuda_error.restype = ctypes.c_int
     lib.nvfp4_last_cuda_error.argtypes = []
+    lib.nvfp4_last_kernel.restype = ctypes.c_char_p
+    lib.nvfp4_last_kernel.argtypes = []
     lib.nvfp4_set_option.restype = ctypes.c_int
     lib.nvfp4_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.nvfp4_release.restype = None
@@ -153,6 +155,10 @@ def nvfp4_status_string(code: int) -> str:
 
 def nvfp4_last_cuda_error() -> int:
     return int(_get().nvfp4_last_cuda_error())
+
+
+def nvfp4_last_kernel() -> str:
+    return _get().nvfp4_last_kernel().decode()
 
 
 def nvfp4_set_option(option: int, value: int) -> None:

@@ -39,6 +39,7 @@ namespace {
 // ------------------------------------------------------------------ state --
 
 std::atomic<int> g_last_cuda_error{0};
+std::atomic<const char *> g_last_kernel{"none"};  // the variant the last call launched
 
 struct Options {
     std::atomic<int64_t> block_n{0};
@@ -593,6 +594,8 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
+    g_last_kernel.store(BN == 128 ? (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<128,2>" : "nvfp4_grouped_gemm_kernel<128,6>")
+                                  : (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<256,2>" : "nvfp4_grouped_gemm_kernel<256,4>"));
     return NVFP4_OK;
 }
 
@@ -635,6 +638,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     nvfp4_pair_gemm_kernel<kPairStages><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
+    g_last_kernel.store("nvfp4_pair_gemm_kernel<5>");
     return NVFP4_OK;
 }
 
@@ -836,6 +840,8 @@ extern "C" const char *nvfp4_status_string(int code)
 }
 
 extern "C" int nvfp4_last_cuda_error(void) { return g_last_cuda_error.load(); }
+
+extern "C" const char *nvfp4_last_kernel(void) { return g_last_kernel.load(); }
 
 extern "C" int nvfp4_set_option(int option, int64_t value)
 {
@@ -1130,5 +1136,6 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
     nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
+    g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,6>");
     return NVFP4_OK;
 }

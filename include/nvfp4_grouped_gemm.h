@@ -131,6 +131,12 @@ const char *nvfp4_status_string(int code);
 /* The cudaError_t value of the last failed CUDA call (0 if none). */
 int nvfp4_last_cuda_error(void);
 
+/* The name of the kernel variant that the last successful GEMM call of this
+ * process launched (for profiles and logs), e.g. "nvfp4_pair_gemm_kernel<5>" or
+ * "nvfp4_grouped_gemm_kernel<128,6>"; "none" before the first launch. A static
+ * string: the caller does not free it. */
+const char *nvfp4_last_kernel(void);
+
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
  *  NVFP4_OPT_CTA_PAIR      : 0 = automatic, 1 = CTA pairs, 2 = single CTAs.

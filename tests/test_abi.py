@@ -87,6 +87,7 @@ def test_trivial_calls_do_not_touch_cuda(nv):
     assert nv.lib.nvfp4_prepack_scales(None, 4, 40, None, None) == -1  # K % 16
     assert nv.lib.nvfp4_prepack_scales(None, 4, 64, None, None) == -1  # null pointers
     assert nv.lib.nvfp4_prepack_scales(8, 4, 64, 256, None) == -2
+    assert nv.nvfp4_last_kernel() == "none"  # nothing launched in a process without a GPU
 
 
 def test_options(nv):

@@ -60,6 +60,17 @@ def test_tiny_workload_every_output():
     d = [DeviceGroup(g) for g in groups]
     run(d)
     check_full(groups, d, "tiny_g2")
+    assert nv.nvfp4_last_kernel().startswith("nvfp4_grouped_gemm_kernel<")  # small sets: single CTAs
+
+
+def test_last_kernel_names_the_variant_that_ran():
+    groups = gen.make_problem_set(3, [130], [512], [256])
+    for pair, name in [(1, "nvfp4_pair_gemm_kernel<5>"), (2, "nvfp4_grouped_gemm_kernel<128,6>")]:
+        nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+        d = [DeviceGroup(g) for g in groups]
+        run(d)
+        assert nv.nvfp4_last_kernel() == name
+        check_full(groups, d, name)
 
 
 RAGGED = dict(seed=77, Ms=[1, 40, 127, 128, 129, 248, 300], Ns=[8, 120, 136, 512, 264, 128, 72],
