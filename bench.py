@@ -308,45 +308,65 @@ def run_ours(args, groups, rank, world, local_rank):
     med_us = statistics.median(per_call_ms) * 1e3
     mean_us_all = reduce_max(mean_us, world)
 
-    # end to end: host buffers, row-major scales, copies inside the timed region
+    # End to end: host buffers, row-major scales, every step's copies inside the timed
+    # region. A step's inputs sit in one pinned host arena and cross in one copy (the host
+    # link carries ~210 GB/s however the bytes are cut, but every copy has a fixed cost),
+    # and its results come back in one copy. Device arenas are double-buffered over three
+    # streams, so step i+1's inputs cross while step i computes and returns its result.
     e2e_steps = max(1, min(args.steps, args.e2e_steps))
-    hostbufs, dbufs, e2e_probs = [], [], []
-    h2d = d2h = 0
-    for g in groups:
-        hA = torch.from_numpy(g.A).pin_memory()
-        hB = torch.from_numpy(g.B).pin_memory()
-        hSFA = torch.from_numpy(g.SFA).pin_memory()
-        hSFB = torch.from_numpy(g.SFB).pin_memory()
-        hC = torch.empty((g.M, g.N), dtype=torch.float16).pin_memory()
-        dA, dB = torch.empty_like(hA, device=dev), torch.empty_like(hB, device=dev)
-        dSFA, dSFB = torch.empty_like(hSFA, device=dev), torch.empty_like(hSFB, device=dev)
-        dC = torch.empty((g.M, g.N), dtype=torch.float16, device=dev)
-        hostbufs.append((hA, hB, hSFA, hSFB, hC))
-        dbufs.append((dA, dB, dSFA, dSFB, dC))
-        e2e_probs.append(nv.problem(dA, dB, dSFA, dSFB, dC, nv.NVFP4_SF_ROWMAJOR))
-        h2d += sum(t.numel() * t.element_size() for t in (hA, hB, hSFA, hSFB))
-        d2h += hC.numel() * hC.element_size()
 
-    def e2e_step():
-        for (hA, hB, hSFA, hSFB, _), (dA, dB, dSFA, dSFB, _) in zip(hostbufs, dbufs):
-            dA.copy_(hA, non_blocking=True)
-            dB.copy_(hB, non_blocking=True)
-            dSFA.copy_(hSFA, non_blocking=True)
-            dSFB.copy_(hSFB, non_blocking=True)
-        nv.nvfp4_grouped_gemm(e2e_probs, stream)
-        for (*_, hC), (*_, dC) in zip(hostbufs, dbufs):
-            hC.copy_(dC, non_blocking=True)
+    def packed(sizes):
+        offs, off = [], 0
+        for n in sizes:
+            offs.append(off)
+            off = (off + n + 255) // 256 * 256
+        return offs, off
 
-    for _ in range(3):
-        e2e_step()
+    in_offs, in_bytes = packed([a.nbytes for g in groups for a in (g.A, g.B, g.SFA, g.SFB)])
+    out_offs, out_bytes = packed([g.M * g.N * 2 for g in groups])
+    h_in = torch.empty(in_bytes, dtype=torch.uint8).pin_memory()
+    for i, arr in enumerate(a for g in groups for a in (g.A, g.B, g.SFA, g.SFB)):
+        h_in[in_offs[i]:in_offs[i] + arr.nbytes].copy_(torch.from_numpy(np.ascontiguousarray(arr).reshape(-1).view(np.uint8)))
+    h_out = torch.empty(out_bytes, dtype=torch.uint8).pin_memory()
+    d_in = [torch.empty(in_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    d_out = [torch.empty(out_bytes, dtype=torch.uint8, device=dev) for _ in range(2)]
+    e2e_probs = []
+    for b in range(2):
+        pi, po = d_in[b].data_ptr(), d_out[b].data_ptr()
+        e2e_probs.append([nv.Nvfp4Problem(g.M, g.N, g.K, nv.NVFP4_SF_ROWMAJOR, pi + in_offs[4 * j], pi + in_offs[4 * j + 1],
+                                          pi + in_offs[4 * j + 2], pi + in_offs[4 * j + 3], po + out_offs[j])
+                          for j, g in enumerate(groups)])
+    h2d, d2h = sum(a.nbytes for g in groups for a in (g.A, g.B, g.SFA, g.SFB)), sum(g.M * g.N * 2 for g in groups)
+    s_in, s_out = torch.cuda.Stream(), torch.cuda.Stream()
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_comp = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+
+    def e2e_step(i):
+        b = i % 2
+        s_in.wait_event(ev_comp[b])  # the GEMM that last read d_in[b] is done
+        with torch.cuda.stream(s_in):
+            d_in[b].copy_(h_in, non_blocking=True)
+        ev_in[b].record(s_in)
+        stream.wait_event(ev_in[b])
+        stream.wait_event(ev_out[b])  # the copy that last read d_out[b] is done
+        nv.nvfp4_grouped_gemm(e2e_probs[b], stream)
+        ev_comp[b].record(stream)
+        s_out.wait_event(ev_comp[b])
+        with torch.cuda.stream(s_out):
+            h_out.copy_(d_out[b], non_blocking=True)
+        ev_out[b].record(s_out)
+
+    for i in range(3):
+        e2e_step(i)
     torch.cuda.synchronize()
     barrier(world)
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for _ in range(e2e_steps):
-        e2e_step()
-    e1.record(stream)
+    e0.record(s_in)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(s_out)  # after the last step's result copy, which follows everything else
     torch.cuda.synchronize()
     barrier(world)
     e2e_us = reduce_max(e0.elapsed_time(e1) * 1e3 / e2e_steps, world)
@@ -354,8 +374,9 @@ def run_ours(args, groups, rank, world, local_rank):
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
     # the e2e result must match the resident-input result bit for bit
-    for (_, _, _, _, C), (*_, hC) in zip(keep, hostbufs):
-        if not torch.equal(C.cpu().view(torch.int16), hC.view(torch.int16)):
+    for j, (g, (_, _, _, _, C)) in enumerate(zip(groups, keep)):
+        hC = h_out[out_offs[j]:out_offs[j] + g.M * g.N * 2].view(torch.int16).view(g.M, g.N)
+        if not torch.equal(C.cpu().view(torch.int16), hC):
             raise RuntimeError("e2e output differs from the resident-input output")
 
     achieved_gbs = nbytes / (mean_us * 1e-6) / 1e9
@@ -398,7 +419,9 @@ def run_ours(args, groups, rank, world, local_rank):
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_us / world, 3), "unit": "us", "steps": e2e_steps, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "gpu_launches_per_step": 2,
-                "path": "pinned host A/B/row-major SFA/SFB -> H2D -> nvfp4_grouped_gemm (prepack + GEMM) -> D2H C"},
+                "path": "one pinned host arena of A/B/row-major SFA/SFB -> one H2D copy -> nvfp4_grouped_gemm (prepack "
+                        "+ GEMM) -> one D2H copy of C; device arenas double-buffered over three streams, so step i+1's "
+                        "copy in overlaps step i's GEMM and copy out"},
     }
     return out
 
