@@ -195,6 +195,18 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     const Table *tab = args.table;
     const uint32_t item_begin = args.list_begin[blockIdx.x];
     const uint32_t item_end = args.list_begin[blockIdx.x + 1];
+    // The producer's first item is read before anything else, so that its latency
+    // overlaps the set-up below.
+    WorkItem first_item{};
+    if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
+        first_item = tab->item(item_begin);
+    // The groups' tensor maps, fetched ahead by the producer warp's lanes in
+    // parallel: one prefetch.tensormap per lane.
+    if (warp == kProducerWarp)
+        for (int i = (int)lane; i < 2 * min(args.num_groups, 64); i += 32) {
+            const GroupEntry &g = tab->group(i / 2);
+            tensormap_prefetch(i % 2 == 0 ? &g.tmap_a : &g.tmap_b);
+        }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -236,10 +248,6 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
-            for (int gi = 0; gi < args.num_groups && gi < 64; ++gi) {
-                tensormap_prefetch(&tab->group(gi).tmap_a);
-                tensormap_prefetch(&tab->group(gi).tmap_b);
-            }
             struct Src {  // where one tile's stages come from
                 const void *tmap_a, *tmap_b;
                 int32_t ya, yb;
@@ -251,7 +259,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             // Everything but the tensor maps' addresses comes from the item itself.
             auto source = [&](uint32_t it) {
                 Src r;
-                const WorkItem w = tab->item(it);
+                const WorkItem w = it == item_begin ? first_item : tab->item(it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: no load
                 r.tmap_a = &ge.tmap_a;
                 r.tmap_b = &ge.tmap_b;

@@ -96,6 +96,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int pair = blockIdx.x >> 1;
     const uint32_t item_begin = args.list_begin[pair];
     const uint32_t item_end = args.list_begin[pair + 1];
+    // The producer's first item is read before anything else, so that its latency
+    // overlaps the set-up below.
+    WorkItem first_item{};
+    if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
+        first_item = tab->item(item_begin);
+    // The groups' tensor maps (A, B, and C for the epilogue's stores), fetched ahead
+    // by the producer warp's lanes in parallel: one prefetch.tensormap per lane.
+    if (warp == kProducerWarp)
+        for (int i = (int)lane; i < 3 * min(args.num_groups, 64); i += 32) {
+            const GroupEntry &g = tab->group(i / 3);
+            tensormap_prefetch(i % 3 == 0 ? &g.tmap_a : i % 3 == 1 ? &g.tmap_b : &g.tmap_c);
+        }
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -112,12 +124,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // The producer needs nothing but the barriers its lane 0 just initialised, so
     // it starts at once (it sends nothing to the peer). The other warps also wait
     // for the TMEM allocation and for the peer's barriers to exist, since the
-    // leader's commits and the peer's arrivals cross the pair.
+    // leader's commits and the peer's arrivals cross the pair. The producer's
+    // cluster arrival is relaxed: the barrier initialisation it did is published
+    // by the other warps' release arrivals, which follow the named barrier (a
+    // cluster-scope release costs about half a microsecond here).
     uint32_t tmem_base = 0;
     if (warp == kProducerWarp) {
         __syncwarp();
         named_barrier_arrive(kSetupBarrier, kThreads);
-        cluster_arrive();
+        cluster_arrive_relaxed();
     } else {
         if (warp == kMmaWarp) {
             tmem_alloc_pair(smem_addr(tmem_base_word), kTmemCols);
@@ -138,14 +153,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
-            for (int gi = 0; gi < args.num_groups && gi < 64; ++gi) {
-                tensormap_prefetch(&tab->group(gi).tmap_a);
-                tensormap_prefetch(&tab->group(gi).tmap_b);
-            }
             uint32_t stage = 0, phase = 0, kiter = 0;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-                const WorkItem w = tab->item(it);
+                const WorkItem w = it == item_begin ? first_item : tab->item(it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: the tensor maps
                 const int kb64 = w.kblocks64;
                 const int32_t ya = w.tile_m * kPairBlockM + (int)rank * 128;
@@ -382,25 +393,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
             } else {
                 // One segment of a split tile, this CTA's 128 rows. Thread e keeps its
-                // elements at float4 index (c*8 + f)*256 + e of the slot.
+                // elements at float4 index (c*8 + f)*256 + e of the slot. Warps whose 32
+                // rows lie past M neither write nor read partials; a CTA half with no row
+                // inside the group skips the whole exchange (the same for every segment
+                // of the tile, so its counter stays untouched).
                 const int e = (warp - kEpilogueWarp0) * 32 + (int)lane;
                 constexpr int kSlotFloats = 128 * kPairBlockN;
+                const bool half_in = w.tile_m * kPairBlockM + (int)rank * 128 < M;  // CTA-uniform
                 float4 *ws = reinterpret_cast<float4 *>(args.workspace + (size_t)(2 * w.ws_slot + (int)rank) * kSlotFloats);
+                if (rows_in) {
 #pragma unroll
-                for (int c = 0; c < kCols / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_load_32cols(t_addr + c * 32, v);
-                    tmem_load_wait();
-                    reg_fence(v);
+                    for (int c = 0; c < kCols / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_load_32cols(t_addr + c * 32, v);
+                        tmem_load_wait();
+                        reg_fence(v);
 #pragma unroll
-                    for (int f = 0; f < 8; ++f)
-                        ws[(c * 8 + f) * 256 + e] = make_float4(__uint_as_float(v[4 * f + 0]), __uint_as_float(v[4 * f + 1]),
-                                                                __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                        for (int f = 0; f < 8; ++f)
+                            ws[(c * 8 + f) * 256 + e] =
+                                make_float4(__uint_as_float(v[4 * f + 0]), __uint_as_float(v[4 * f + 1]),
+                                            __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0)
                     release_accumulator();
+                if (!half_in)
+                    continue;
                 __threadfence();
                 named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
                 if (e == 0)
@@ -412,11 +432,20 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const float4 *ws0 = reinterpret_cast<const float4 *>(
                         args.workspace + (size_t)(2 * (w.ws_slot - w.seg) + (int)rank) * kSlotFloats);
                     constexpr size_t kSegStride = 2 * (size_t)kSlotFloats / 4;  // float4 units
+                    // Each partial is read once, here: its L2 lines are then dropped, so
+                    // they are never written back to DRAM. Lane l < 4 drops the 128-byte
+                    // line of lanes 8l .. 8l+7, after the whole warp has read it.
+                    auto drop = [&](const float4 *wp, int c) {
+                        __syncwarp();
+                        if (lane < 4) {
+#pragma unroll
+                            for (int f = 0; f < 8; ++f)
+                                discard_l2_line(&wp[(c * 8 + f) * 256 + (e - (int)lane) + 8 * (int)lane]);
+                        }
+                    };
                     if (rows_in) {
 #pragma unroll 1
                         for (int c = 0; c < kCols / 32; ++c) {
-                            if (n0 + c * 32 >= N)
-                                break;
                             float4 acc[8];
 #pragma unroll
                             for (int f = 0; f < 8; ++f)
@@ -430,14 +459,18 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                                 for (int f = 0; f < 8; ++f)
                                     acc[f].x += q[f].x, acc[f].y += q[f].y, acc[f].z += q[f].z, acc[f].w += q[f].w;
+                                drop(wp, c);
                             }
-                            uint32_t h[16];
+                            drop(ws0, c);
+                            if (n0 + c * 32 < N) {
+                                uint32_t h[16];
 #pragma unroll
-                            for (int f = 0; f < 8; ++f) {
-                                h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
-                                h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
+                                for (int f = 0; f < 8; ++f) {
+                                    h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
+                                    h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
+                                }
+                                store_chunk(&ge.tmap_c, n0 + c * 32, m_row0, h);
                             }
-                            store_chunk(&ge.tmap_c, n0 + c * 32, m_row0, h);
                         }
                     }
                     if (e == 0)

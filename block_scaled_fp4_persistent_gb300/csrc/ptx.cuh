@@ -59,6 +59,12 @@ __device__ __forceinline__ void cluster_sync()
 // The two halves of cluster_sync, for a warp that arrives early and waits later.
 __device__ __forceinline__ void cluster_arrive() { asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory"); }
 __device__ __forceinline__ void cluster_wait() { asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory"); }
+// An arrival that releases nothing: for a warp whose writes other warps of its CTA
+// publish with their own (release) arrivals.
+__device__ __forceinline__ void cluster_arrive_relaxed()
+{
+    asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
 
 // The shared::cluster address of the object at shared::cta address `addr` in CTA `rank` of the cluster.
 __device__ __forceinline__ uint32_t cluster_map(uint32_t addr, uint32_t rank)
@@ -198,6 +204,13 @@ __device__ __forceinline__ void bulk_wait_group()
 // Makes this thread's generic-proxy writes to shared memory visible to the async
 // proxy (a TMA store that reads them).
 __device__ __forceinline__ void fence_proxy_async_smem() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Drops a 128-byte line from L2 without writing it back; its contents become
+// undefined. addr 128-byte aligned.
+__device__ __forceinline__ void discard_l2_line(const void *addr)
+{
+    asm volatile("discard.global.L2 [%0], 128;" ::"l"(addr) : "memory");
+}
 
 // Prefetch of a 2-D tile of the tensor map into L2 (no shared memory, no completion).
 __device__ __forceinline__ void tma_prefetch_2d(const void *tmap, int32_t x, int32_t y)
