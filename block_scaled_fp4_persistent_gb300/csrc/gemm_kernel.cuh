@@ -15,9 +15,10 @@
 //               scale slot with tcgen05.st, in the layout that
 //               tcgen05.cp .32x128b.warpx4 would produce.
 //   warps 6-13  epilogue. Two warps per TMEM lane quarter, each owning BN/2
-//               columns. They drain the accumulator to registers (converting to
-//               fp16 on the way), free it for the next tile's MMAs, then store the
-//               rows that lie inside the group.
+//               columns. They drain the accumulator 32 columns at a time, convert to
+//               fp16, and send each 32 x 32 block out through a swizzled shared-memory
+//               buffer and a TMA store (which clips rows past M and columns past N);
+//               the accumulator is freed for the next tile after the last TMEM read.
 //
 // Why this shape. Measurements on this GPU drove it:
 //  * One tcgen05.cp of a 512-byte scale block costs about as much tensor-pipe
@@ -60,6 +61,7 @@ constexpr int kBlockK = 256;             // K per stage = 128 bytes of E2M1 per 
 constexpr int kRowBytes = kBlockK / 2;   // 128
 constexpr int kScaleBlockBytes = 512;    // scales of 128 rows x 64 K
 constexpr uint32_t kTmemCols = 512;
+constexpr int kEpiBufBytes = 32 * 64;    // one epilogue staging buffer: 32 rows x 64 bytes
 
 // Roles reported in the status words.
 constexpr int kRoleProducer = 0, kRoleMma = 1, kRoleEpilogue = 2, kRoleTeardown = 3, kRoleScales = 4;
@@ -79,9 +81,12 @@ struct Layout {
     static constexpr int kOffSfa = kABytes + kBBytes;
     static constexpr int kOffSfb = kOffSfa + kSfaBytes;            // half h, k-block j at + (4h + j) * 512
     static constexpr int kRingBytes = STAGES * kStageBytes;
+    // epilogue staging: two buffers per epilogue warp (see EpilogueStager)
+    static constexpr int kOffEpi = kRingBytes;
+    static constexpr int kEpiBytes = kEpilogueWarps * 2 * kEpiBufBytes;
     // barriers: full[S], empty[S], sf_full[S], acc_full, acc_empty, drain, then the TMEM base word
     static constexpr int kBarBytes = (3 * STAGES + 3) * 8 + 16;
-    static constexpr int kSmemBytes = 1024 + kRingBytes + kBarBytes + 64;  // the SharedState lives in the last 64
+    static constexpr int kSmemBytes = 1024 + kRingBytes + kEpiBytes + kBarBytes + 64;  // the SharedState lives in the last 64
     // TMEM columns: the accumulator at 0 .. BN-1, then one scale slot per stage:
     //   SFA at +0 .. 15 (k-block j at +4j),
     //   SFB at +16 .. (k-block j at +16 + 4*kHalves*j; its half h at +4h within that).
@@ -171,6 +176,45 @@ __device__ __forceinline__ uint32_t pack_half2(uint32_t lo, uint32_t hi)
     return *reinterpret_cast<uint32_t *>(&h);
 }
 
+// An epilogue warp's way out for C: two 2 KB shared-memory buffers of 32 rows x 64
+// bytes (32 fp16 columns), alternated, each the source of one TMA store of a
+// 32 x 32 box. Before a buffer is rewritten, the store that read it two chunks ago
+// must have finished reading shared memory. Rows go in with the 64-byte swizzle
+// (16-byte chunk j of row r at position j ^ ((r >> 1) & 3)), which is what the
+// tensor map expects and keeps the warp's writes free of bank conflicts.
+struct EpilogueStager {
+    uint8_t *bufs;  // 2 * kEpiBufBytes, 1024-byte aligned
+    uint32_t n = 0;
+
+    // Row `lane` of the box comes from h[0..15]; (x, y) is the box's first column and row.
+    __device__ __forceinline__ void store(const CUtensorMap *tmap, int x, int y, const uint32_t *h, uint32_t lane)
+    {
+        uint8_t *buf = bufs + (n & 1) * kEpiBufBytes;
+        ++n;
+        if (lane == 0)
+            bulk_wait_group_read<1>();
+        __syncwarp();
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+            *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
+                make_uint4(h[4 * j + 0], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            tma_store_2d(tmap, x, y, smem_addr(buf));
+            bulk_commit_group();
+        }
+    }
+
+    // Every store must be complete before the CTA exits.
+    __device__ __forceinline__ void finish(uint32_t lane)
+    {
+        if (lane == 0)
+            bulk_wait_group<0>();
+        __syncwarp();
+    }
+};
+
 template <int BN, int STAGES>
 __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const __grid_constant__ KernelArgs args)
 {
@@ -180,7 +224,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     // 1024-byte alignment for the 128-byte swizzle pattern of the operand tiles
     uint8_t *smem = reinterpret_cast<uint8_t *>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t *ring = smem;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kRingBytes);
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + L::kOffEpi + L::kEpiBytes);
     uint64_t *full = bars;
     uint64_t *empty = bars + STAGES;
     uint64_t *sf_full = bars + 2 * STAGES;
@@ -467,68 +511,69 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     } else {
         // ------------------------------------------------------ epilogue
         // Warp w owns TMEM lane quarter w % 4 and the column half (w - 6) / 4 of the
-        // accumulator: output row tile_m*128 + 32*(w % 4) + lane, columns
-        // half*BN/2 .. half*BN/2 + BN/2 - 1 of the tile.
+        // accumulator: output rows tile_m*128 + 32*(w % 4) + lane, columns
+        // half*BN/2 .. half*BN/2 + BN/2 - 1 of the tile. C leaves through staged TMA
+        // stores, which clip rows past M and columns past N.
         const int quarter = warp % 4;  // warps 6..13 -> quarters 2,3,0,1,2,3,0,1
         const int chalf = (warp - kEpilogueWarp0) / 4;
         constexpr int kCols = BN / 2;
         const uint32_t t_addr = tmem_base + ((uint32_t)(quarter * 32) << 16) + chalf * kCols;
-        const int row_in_tile = quarter * 32 + (int)lane;
+        EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = tab->item(it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
-            __half *const C = ge.C;
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
                 break;
             acc_phase ^= 1u;
             tc_fence_after();
-            const int m = w.tile_m * kBlockM + row_in_tile;
+            const int m_row0 = w.tile_m * kBlockM + quarter * 32;  // first of this warp's 32 rows
+            const bool rows_in = m_row0 < M;                       // warp-uniform
             const int n0 = w.tile_n * BN + chalf * kCols;
             if (w.split < 0) {
-                // whole tile: drain 32 columns at a time, packed to fp16 pairs as they arrive
-                uint32_t hv[kCols / 2];
-#pragma unroll
+                // whole tile: 32 columns at a time, TMEM -> fp16 -> staging -> TMA store
+#pragma unroll 1
                 for (int c = 0; c < kCols / 32; ++c) {
                     uint32_t v[32];
                     tmem_load_32cols(t_addr + c * 32, v);
                     tmem_load_wait();
                     reg_fence(v);
+                    if (c == kCols / 32 - 1) {  // this warp's last read of the accumulator
+                        tc_fence_before();
+                        __syncwarp();
+                        if (lane == 0)
+                            mbar_arrive(smem_addr(acc_empty));
+                    }
+                    if (rows_in && n0 + c * 32 < N) {
+                        uint32_t h[16];
 #pragma unroll
-                    for (int i = 0; i < 16; ++i)
-                        hv[c * 16 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0)
-                    mbar_arrive(smem_addr(acc_empty));
-                if (m < M) {
-                    __half *crow = C + (size_t)m * N + n0;
-#pragma unroll
-                    for (int q = 0; q < kCols / 8; ++q) {
-                        if (n0 + q * 8 < N)
-                            *reinterpret_cast<uint4 *>(crow + q * 8) =
-                                make_uint4(hv[4 * q + 0], hv[4 * q + 1], hv[4 * q + 2], hv[4 * q + 3]);
+                        for (int i = 0; i < 16; ++i)
+                            h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
+                        out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
                     }
                 }
             } else {
-                // one segment of a split tile: its fp32 partial goes to the workspace slot.
+                // One segment of a split tile: its fp32 partial goes to the workspace slot.
                 // Thread e of the epilogue keeps its elements at float4 index (c*8 + f)*256 + e
                 // of the slot, so every store and load of a warp covers 512 contiguous bytes.
+                // Warps whose 32 rows lie past M neither write nor read partials.
                 const int e = (warp - kEpilogueWarp0) * 32 + (int)lane;
                 constexpr int kSlotFloats = kBlockM * BN;
                 float4 *ws = reinterpret_cast<float4 *>(args.workspace + (size_t)w.ws_slot * kSlotFloats);
+                if (rows_in) {
 #pragma unroll
-                for (int c = 0; c < kCols / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_load_32cols(t_addr + c * 32, v);
-                    tmem_load_wait();
-                    reg_fence(v);
+                    for (int c = 0; c < kCols / 32; ++c) {
+                        uint32_t v[32];
+                        tmem_load_32cols(t_addr + c * 32, v);
+                        tmem_load_wait();
+                        reg_fence(v);
 #pragma unroll
-                    for (int f = 0; f < 8; ++f)
-                        ws[(c * 8 + f) * 256 + e] = make_float4(__uint_as_float(v[4 * f + 0]), __uint_as_float(v[4 * f + 1]),
-                                                                __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                        for (int f = 0; f < 8; ++f)
+                            ws[(c * 8 + f) * 256 + e] =
+                                make_float4(__uint_as_float(v[4 * f + 0]), __uint_as_float(v[4 * f + 1]),
+                                            __uint_as_float(v[4 * f + 2]), __uint_as_float(v[4 * f + 3]));
+                    }
                 }
                 tc_fence_before();
                 __syncwarp();
@@ -545,8 +590,18 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     __threadfence();
                     const float4 *ws0 = reinterpret_cast<const float4 *>(args.workspace +
                                                                          (size_t)(w.ws_slot - w.seg) * kSlotFloats);
-                    if (m < M) {
-                        __half *crow = C + (size_t)m * N + n0;
+                    // Each partial is read once, here: its L2 lines are then dropped, so they
+                    // are never written back to DRAM. Lane l < 4 drops the 128-byte line of
+                    // lanes 8l .. 8l+7, after the whole warp has read it.
+                    auto drop = [&](const float4 *wp, int c) {
+                        __syncwarp();
+                        if (lane < 4) {
+#pragma unroll
+                            for (int f = 0; f < 8; ++f)
+                                discard_l2_line(&wp[(c * 8 + f) * 256 + (e - (int)lane) + 8 * (int)lane]);
+                        }
+                    };
+                    if (rows_in) {
 #pragma unroll 1
                         for (int c = 0; c < kCols / 32; ++c) {
                             // 32 columns at a time, eight independent loads per segment in
@@ -565,14 +620,17 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
 #pragma unroll
                                 for (int f = 0; f < 8; ++f)
                                     acc[f].x += q[f].x, acc[f].y += q[f].y, acc[f].z += q[f].z, acc[f].w += q[f].w;
+                                drop(wp, c);
                             }
+                            drop(ws0, c);
+                            if (n0 + c * 32 < N) {
+                                uint32_t h[16];
 #pragma unroll
-                            for (int f = 0; f < 8; ++f) {
-                                const int col = c * 32 + f * 4;
-                                if (n0 + col < N)
-                                    *reinterpret_cast<uint2 *>(crow + col) =
-                                        make_uint2(pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y)),
-                                                   pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w)));
+                                for (int f = 0; f < 8; ++f) {
+                                    h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
+                                    h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
+                                }
+                                out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
                             }
                         }
                     }
@@ -582,6 +640,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);  // sh->last is read before it is rewritten
             }
         }
+        out.finish(lane);
     }
 
     tc_fence_before();

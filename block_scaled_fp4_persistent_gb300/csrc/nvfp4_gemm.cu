@@ -56,8 +56,8 @@ constexpr int kMaxDevices = 64;
 // Kernel variants: BLOCK_N 128 or 256, each with the deepest ring that fits in
 // shared memory, or a 2-stage ring (for tests).
 constexpr int kDefaultBlockN = 128;
-constexpr int kDeepStages128 = 6;  // 6 x 36 KB
-constexpr int kDeepStages256 = 4;  // 4 x 54 KB
+constexpr int kDeepStages128 = 5;  // 5 x 36 KB, + 32 KB of epilogue staging
+constexpr int kDeepStages256 = 3;  // 3 x 54 KB, + 32 KB of epilogue staging
 constexpr int kDefaultStages = kDefaultBlockN == 256 ? kDeepStages256 : kDeepStages128;
 // The CTA-pair kernel: 256 x 256 tiles, 5 x 38 KB ring (its TMEM holds 5 scale slots).
 constexpr int kPairStages = 5;
@@ -496,7 +496,7 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         int rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, (uint64_t)a.M, kBlockM);
         if (!rc)
             rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, pair ? 128u : (uint32_t)block_n);
-        if (!rc && pair)
+        if (!rc)
             rc = encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
         if (rc) {
             cudaFreeHost(t.host);
@@ -594,8 +594,9 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
-    g_last_kernel.store(BN == 128 ? (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<128,2>" : "nvfp4_grouped_gemm_kernel<128,6>")
-                                  : (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<256,2>" : "nvfp4_grouped_gemm_kernel<256,4>"));
+    static_assert(kDeepStages128 == 5 && kDeepStages256 == 3, "kernel names below");
+    g_last_kernel.store(BN == 128 ? (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<128,2>" : "nvfp4_grouped_gemm_kernel<128,5>")
+                                  : (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<256,2>" : "nvfp4_grouped_gemm_kernel<256,3>"));
     return NVFP4_OK;
 }
 
@@ -1097,6 +1098,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         int rc = encode_operand_map(&e.tmap_a, p.A, (uint64_t)p.K / 2, (uint64_t)p.M, kBlockM);
         if (!rc)
             rc = encode_operand_map(&e.tmap_b, p.B, (uint64_t)p.K / 2, (uint64_t)p.N, (uint32_t)BN);
+        if (!rc)
+            rc = encode_output_map(&e.tmap_c, p.C, (uint64_t)p.M, (uint64_t)p.N);
         if (rc)
             return rc;
         e.sfa = static_cast<const uint8_t *>(p.SFA);
@@ -1136,6 +1139,6 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
     nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
-    g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,6>");
+    g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");
     return NVFP4_OK;
 }

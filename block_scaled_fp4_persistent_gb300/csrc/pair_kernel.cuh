@@ -55,9 +55,7 @@ struct PairLayout {
     static constexpr int kOffSfa = kABytes + kBBytes;
     static constexpr int kOffSfb = kOffSfa + kSfaBytes;          // half h, k-block j at + (4h + j) * 512
     static constexpr int kRingBytes = STAGES * kStageBytes;
-    // Epilogue staging: per epilogue warp two 2 KB buffers of 32 rows x 32 fp16
-    // columns (64-byte rows, 64-byte swizzle), the source of its TMA stores of C.
-    static constexpr int kEpiBufBytes = 32 * 64;
+    // epilogue staging: two buffers per epilogue warp (see EpilogueStager)
     static constexpr int kOffEpi = kRingBytes;
     static constexpr int kEpiBytes = kEpilogueWarps * 2 * kEpiBufBytes;
     static constexpr int kBarBytes = (3 * STAGES + 3) * 8 + 16;
@@ -332,30 +330,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             else
                 mbar_arrive_remote_relaxed(acc_empty_leader);
         };
-        // C goes out through this warp's two staging buffers: 32 rows x 32 columns per
-        // TMA store, alternating buffers. Before a buffer is rewritten, the store that
-        // read it two chunks ago must have finished reading shared memory.
-        uint8_t *const epi = smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * L::kEpiBufBytes;
-        uint32_t chunk_no = 0;
-        auto store_chunk = [&](const CUtensorMap *tmap_c, int x, int y, const uint32_t (&h)[16]) {
-            uint8_t *buf = epi + (chunk_no & 1) * L::kEpiBufBytes;
-            ++chunk_no;
-            if (lane == 0)
-                bulk_wait_group_read<1>();
-            __syncwarp();
-            // row `lane` = 64 bytes = four 16-byte chunks, chunk j at (j ^ ((row >> 1) & 3)):
-            // the 64-byte swizzle, which also keeps the warp's writes free of bank conflicts
-#pragma unroll
-            for (int j = 0; j < 4; ++j)
-                *reinterpret_cast<uint4 *>(buf + lane * 64 + ((j ^ ((lane >> 1) & 3)) << 4)) =
-                    make_uint4(h[4 * j + 0], h[4 * j + 1], h[4 * j + 2], h[4 * j + 3]);
-            fence_proxy_async_smem();
-            __syncwarp();
-            if (lane == 0) {
-                tma_store_2d(tmap_c, x, y, smem_addr(buf));
-                bulk_commit_group();
-            }
-        };
+        // C goes out through this warp's two staging buffers and TMA stores
+        EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = tab->item(it);
@@ -388,7 +364,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                         for (int i = 0; i < 16; ++i)
                             h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
-                        store_chunk(&ge.tmap_c, n0 + c * 32, m_row0, h);
+                        out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
                     }
                 }
             } else {
@@ -469,7 +445,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
                                     h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
                                 }
-                                store_chunk(&ge.tmap_c, n0 + c * 32, m_row0, h);
+                                out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
                             }
                         }
                     }
@@ -479,10 +455,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 named_barrier_sync(kEpilogueBarrier, kEpilogueWarps * 32);
             }
         }
-        // every store of C must be complete before the CTA exits
-        if (lane == 0)
-            bulk_wait_group<0>();
-        __syncwarp();
+        out.finish(lane);
     }
 
     if (warp == kProducerWarp)

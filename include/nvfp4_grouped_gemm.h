@@ -133,7 +133,7 @@ int nvfp4_last_cuda_error(void);
 
 /* The name of the kernel variant that the last successful GEMM call of this
  * process launched (for profiles and logs), e.g. "nvfp4_pair_gemm_kernel<5>" or
- * "nvfp4_grouped_gemm_kernel<128,6>"; "none" before the first launch. A static
+ * "nvfp4_grouped_gemm_kernel<128,5>"; "none" before the first launch. A static
  * string: the caller does not free it. */
 const char *nvfp4_last_kernel(void);
 
@@ -152,7 +152,7 @@ const char *nvfp4_last_kernel(void);
  *  NVFP4_OPT_BLOCK_N       : 0 = automatic (128), or 128 or 256: the width of
  *                             the single-CTA output tiles (and the MMA's N)
  *  NVFP4_OPT_STAGES        : 0 = automatic (the deepest shared-memory ring that
- *                             fits: 6 stages at BLOCK_N 128, 4 at 256, 5 for
+ *                             fits: 5 stages at BLOCK_N 128, 3 at 256, 5 for
  *                             pairs), or 2 (single CTAs)
  *  NVFP4_OPT_MAX_CTAS      : 0 = one CTA per SM, or an upper bound on the grid
  *                             (pairs: on twice the number of pairs)

@@ -65,7 +65,7 @@ def test_tiny_workload_every_output():
 
 def test_last_kernel_names_the_variant_that_ran():
     groups = gen.make_problem_set(3, [130], [512], [256])
-    for pair, name in [(1, "nvfp4_pair_gemm_kernel<5>"), (2, "nvfp4_grouped_gemm_kernel<128,6>")]:
+    for pair, name in [(1, "nvfp4_pair_gemm_kernel<5>"), (2, "nvfp4_grouped_gemm_kernel<128,5>")]:
         nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
         d = [DeviceGroup(g) for g in groups]
         run(d)
