@@ -97,6 +97,15 @@ struct Layout {
     static_assert(BN + STAGES * kSfColsPerStage <= (int)kTmemCols, "TMEM budget");
 };
 
+// Item `it` of the table. Read through the items pointer passed with the launch, it
+// is one load: through the table header's offset it would be two dependent ones,
+// each a DRAM round trip at the start of a launch.
+__device__ __forceinline__ WorkItem global_item(const KernelArgs &args, uint32_t it)
+{
+    const int4 *p = args.items + 4 * (size_t)it;
+    return unpack_item(p[0], p[1], p[2], p[3]);
+}
+
 struct SharedState {
     volatile int abort;  // set by the first role that gives up a wait
     volatile int last;   // epilogue: this CTA completes the split tile being stored
@@ -243,7 +252,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     // overlaps the set-up below.
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
-        first_item = tab->item(item_begin);
+        first_item = global_item(args, item_begin);
     // The groups' tensor maps, fetched ahead by the producer warp's lanes in
     // parallel: one prefetch.tensormap per lane.
     if (warp == kProducerWarp)
@@ -303,7 +312,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             // Everything but the tensor maps' addresses comes from the item itself.
             auto source = [&](uint32_t it) {
                 Src r;
-                const WorkItem w = it == item_begin ? first_item : tab->item(it);
+                const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: no load
                 r.tmap_a = &ge.tmap_a;
                 r.tmap_b = &ge.tmap_b;
@@ -404,7 +413,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             uint32_t sf = tmem_sf;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-                const WorkItem w = tab->item(it);
+                const WorkItem w = global_item(args, it);
                 const int kb64 = w.kblocks64;
                 // the epilogue warps must have drained the previous tile's accumulator
                 if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
@@ -468,7 +477,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-            const WorkItem w = tab->item(it);
+            const WorkItem w = global_item(args, it);
             for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                 if (!warp_wait_phase(smem_addr(&full[stage]), phase, sh, args, kRoleScales, (int)it, kb)) {
                     ok = false;
@@ -521,7 +530,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
-            const WorkItem w = tab->item(it);
+            const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
@@ -532,26 +541,29 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             const bool rows_in = m_row0 < M;                       // warp-uniform
             const int n0 = w.tile_n * BN + chalf * kCols;
             if (w.split < 0) {
-                // whole tile: 32 columns at a time, TMEM -> fp16 -> staging -> TMA store
-#pragma unroll 1
-                for (int c = 0; c < kCols / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_load_32cols(t_addr + c * 32, v);
+                // whole tile: the warp's columns TMEM -> fp16 registers, the accumulator
+                // released (the next tile's MMAs wait for it), then 32 columns at a time
+                // -> staging -> TMA store: the release never waits for the store path.
+                uint32_t h[kCols / 32][16];
+#pragma unroll
+                for (int c = 0; c < kCols / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_load_16cols(t_addr + c * 16, v);
                     tmem_load_wait();
                     reg_fence(v);
-                    if (c == kCols / 32 - 1) {  // this warp's last read of the accumulator
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            mbar_arrive(smem_addr(acc_empty));
-                    }
-                    if (rows_in && n0 + c * 32 < N) {
-                        uint32_t h[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
-                        out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        h[c / 2][(c % 2) * 8 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    mbar_arrive(smem_addr(acc_empty));
+                if (rows_in) {
+#pragma unroll
+                    for (int c = 0; c < kCols / 32; ++c)
+                        if (n0 + c * 32 < N)
+                            out.store(&ge.tmap_c, n0 + c * 32, m_row0, h[c], lane);
                 }
             } else {
                 // One segment of a split tile: its fp32 partial goes to the workspace slot.

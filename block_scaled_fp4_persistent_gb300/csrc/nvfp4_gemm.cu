@@ -96,6 +96,13 @@ struct CachedTable {
     int variant = 0;  // the kernel variant the table was built for
     std::vector<uint32_t> list_begin;  // the table's cta_begin, passed again with each launch
 };
+// The device address of a cached table's work items.
+const int4 *table_items(const CachedTable &t)
+{
+    const TableHeader *th = static_cast<const TableHeader *>(t.host);
+    return reinterpret_cast<const int4 *>(static_cast<const uint8_t *>(t.dev) + th->off_items);
+}
+
 std::list<CachedTable> g_tables;  // most recently used first
 std::unordered_map<uint64_t, std::list<CachedTable>::iterator> g_table_index;
 
@@ -583,6 +590,7 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     using L = Layout<BN, STAGES>;
     KernelArgs args{};
     args.table = static_cast<const Table *>(t.dev);
+    args.items = table_items(t);
     args.status = ds.status;
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
     args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
@@ -629,6 +637,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     using L = PairLayout<kPairStages>;
     KernelArgs args{};
     args.table = static_cast<const Table *>(t.dev);
+    args.items = table_items(t);
     args.status = ds.status;
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
     args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
@@ -1129,6 +1138,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
 
     KernelArgs args{};
     args.table = dtable;
+    args.items = reinterpret_cast<const int4 *>(reinterpret_cast<const uint8_t *>(dtable) + off_items);
     args.status = dstatus;
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
     args.fault_skip_load = -1;

@@ -98,7 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // overlaps the set-up below.
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
-        first_item = tab->item(item_begin);
+        first_item = global_item(args, item_begin);
     // The groups' tensor maps (A, B, and C for the epilogue's stores), fetched ahead
     // by the producer warp's lanes in parallel: one prefetch.tensormap per lane.
     if (warp == kProducerWarp)
@@ -154,7 +154,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t stage = 0, phase = 0, kiter = 0;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-                const WorkItem w = it == item_begin ? first_item : tab->item(it);
+                const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: the tensor maps
                 const int kb64 = w.kblocks64;
                 const int32_t ya = w.tile_m * kPairBlockM + (int)rank * 128;
@@ -213,7 +213,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             uint32_t sf = tmem_sf;
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-                const WorkItem w = tab->item(it);
+                const WorkItem w = global_item(args, it);
                 const int kb64 = w.kblocks64;
                 if (!wait_phase(smem_addr(acc_empty), acc_phase ^ 1u, sh, args, kRoleMma, (int)it, -1)) {
                     ok = false;
@@ -271,7 +271,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         uint32_t stage = 0, phase = 0;
         bool ok = true;
         for (uint32_t it = item_begin; ok && it < item_end; ++it) {
-            const WorkItem w = tab->item(it);
+            const WorkItem w = global_item(args, it);
             for (int kb = w.kb_begin; kb < w.kb_end; ++kb) {
                 if (!warp_wait_phase(smem_addr(&full[stage]), phase, sh, args, kRoleScales, (int)it, kb)) {
                     ok = false;
@@ -334,7 +334,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
-            const WorkItem w = tab->item(it);
+            const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
@@ -346,26 +346,29 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const int m_row0 = m - (int)lane;    // first of this warp's 32 rows
             const bool rows_in = m_row0 < M;     // warp-uniform
             if (w.split < 0) {
-                // whole tile: 32 columns at a time, TMEM -> fp16 -> staging -> TMA store
-#pragma unroll 1
-                for (int c = 0; c < kCols / 32; ++c) {
-                    uint32_t v[32];
-                    tmem_load_32cols(t_addr + c * 32, v);
+                // whole tile: the warp's columns TMEM -> fp16 registers, the accumulator
+                // released (the next tile's MMAs wait for it), then 32 columns at a time
+                // -> staging -> TMA store: the release never waits for the store path.
+                uint32_t h[kCols / 32][16];
+#pragma unroll
+                for (int c = 0; c < kCols / 16; ++c) {
+                    uint32_t v[16];
+                    tmem_load_16cols(t_addr + c * 16, v);
                     tmem_load_wait();
                     reg_fence(v);
-                    if (c == kCols / 32 - 1) {  // this warp's last read of the accumulator
-                        tc_fence_before();
-                        __syncwarp();
-                        if (lane == 0)
-                            release_accumulator();
-                    }
-                    if (rows_in && n0 + c * 32 < N) {
-                        uint32_t h[16];
 #pragma unroll
-                        for (int i = 0; i < 16; ++i)
-                            h[i] = pack_half2(v[2 * i], v[2 * i + 1]);
-                        out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
-                    }
+                    for (int i = 0; i < 8; ++i)
+                        h[c / 2][(c % 2) * 8 + i] = pack_half2(v[2 * i], v[2 * i + 1]);
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0)
+                    release_accumulator();
+                if (rows_in) {
+#pragma unroll
+                    for (int c = 0; c < kCols / 32; ++c)
+                        if (n0 + c * 32 < N)
+                            out.store(&ge.tmap_c, n0 + c * 32, m_row0, h[c], lane);
                 }
             } else {
                 // One segment of a split tile, this CTA's 128 rows. Thread e keeps its

@@ -65,6 +65,18 @@ constexpr int32_t kItemB2 = 4;       // rows 128..255 of the tile's B rows exist
 
 static_assert(sizeof(WorkItem) == 64, "WorkItem is read as four int4");
 
+// An item from its four int4 words (the layout of WorkItem).
+__host__ __device__ inline WorkItem unpack_item(int4 a, int4 b, int4 c, int4 d)
+{
+    WorkItem w;
+    w.group = a.x, w.tile_m = a.y, w.tile_n = a.z, w.kb_begin = a.w;
+    w.kb_end = b.x, w.split = b.y, w.seg = b.z, w.nseg = b.w;
+    w.ws_slot = c.x, w.kblocks64 = c.y, w.flags = c.z, w.reserved = c.w;
+    w.sfa = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.x | ((uint64_t)(uint32_t)d.y << 32));
+    w.sfb = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.z | ((uint64_t)(uint32_t)d.w << 32));
+    return w;
+}
+
 struct alignas(128) TableHeader {
     int32_t num_groups;
     int32_t num_items;
@@ -85,18 +97,6 @@ struct Table {
     {
         return reinterpret_cast<const uint32_t *>(reinterpret_cast<const char *>(this) + h.off_cta_begin)[c];
     }
-    __host__ __device__ WorkItem item(uint32_t i) const
-    {
-        const int4 *p = reinterpret_cast<const int4 *>(reinterpret_cast<const char *>(this) + h.off_items) + 4 * i;
-        const int4 a = p[0], b = p[1], c = p[2], d = p[3];
-        WorkItem w;
-        w.group = a.x, w.tile_m = a.y, w.tile_n = a.z, w.kb_begin = a.w;
-        w.kb_end = b.x, w.split = b.y, w.seg = b.z, w.nseg = b.w;
-        w.ws_slot = c.x, w.kblocks64 = c.y, w.flags = c.z, w.reserved = c.w;
-        w.sfa = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.x | ((uint64_t)(uint32_t)d.y << 32));
-        w.sfb = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.z | ((uint64_t)(uint32_t)d.w << 32));
-        return w;
-    }
     int num_groups_host() const { return h.num_groups; }
 };
 
@@ -105,6 +105,7 @@ constexpr int kMaxLists = 256;
 
 struct KernelArgs {
     const Table *table;
+    const int4 *items;      // the table's work items (four int4 each), so that no read waits for the header
     // List l holds items list_begin[l] .. list_begin[l+1]-1. A copy of the table's
     // cta_begin array, passed with the launch so that no CTA waits for it.
     uint32_t list_begin[kMaxLists + 1];
