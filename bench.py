@@ -23,7 +23,8 @@ Timing (ours):
    `value` is the mean over K calls; median, min and max are also reported.
  * e2e runs the same call through the public API from pinned HOST buffers with
    row-major scales. Each timed step copies A, B, SFA and SFB host->device,
-   runs the prepack and the GEMM, and copies C device->host.
+   runs the GEMM (which reads row-major scales itself where K % 256 == 0, else
+   after a prepack launch), and copies C device->host.
  * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
    scaling; the path has no exchange step). Timing is the max over ranks, and
    `value` = that time divided by N (aggregate time per grouped call).
@@ -370,6 +371,7 @@ def run_ours(args, groups, rank, world, local_rank):
     torch.cuda.synchronize()
     barrier(world)
     e2e_us = reduce_max(e0.elapsed_time(e1) * 1e3 / e2e_steps, world)
+    e2e_launches = nv.nvfp4_last_launches()  # kernels per grouped call on this path
     st, detail = nv.nvfp4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
@@ -418,10 +420,11 @@ def run_ours(args, groups, rank, world, local_rank):
         "timed_region_wall_s": round(wall, 3),
         "clocks": clocks.summary(),
         "e2e": {"value": round(e2e_us / world, 3), "unit": "us", "steps": e2e_steps, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "gpu_launches_per_step": 2,
-                "path": "one pinned host arena of A/B/row-major SFA/SFB -> one H2D copy -> nvfp4_grouped_gemm (prepack "
-                        "+ GEMM) -> one D2H copy of C; device arenas double-buffered over three streams, so step i+1's "
-                        "copy in overlaps step i's GEMM and copy out"},
+                "d2h_bytes_per_step": d2h, "gpu_launches_per_step": e2e_launches,
+                "path": "one pinned host arena of A/B/row-major SFA/SFB -> one H2D copy -> nvfp4_grouped_gemm (the GEMM "
+                        "kernel reads the row-major scales itself where K % 256 == 0, else a prepack launch first) -> "
+                        "one D2H copy of C; device arenas double-buffered over three streams, so step i+1's copy in "
+                        "overlaps step i's GEMM and copy out"},
     }
     return out
 

@@ -10,7 +10,8 @@ been built, the first call raises ImportError. Build it with
 
 Names match the C ABI: ``nvfp4_grouped_gemm``, ``nvfp4_prepack_scales``,
 ``nvfp4_prepacked_scale_bytes``, ``nvfp4_device_status``,
-``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_last_kernel``, ``nvfp4_set_option`` and
+``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_last_kernel``, ``nvfp4_last_launches``,
+``nvfp4_set_option`` and
 ``nvfp4_release``.
 """
 from __future__ import annotations
@@ -41,6 +42,7 @@ NVFP4_OPT_FAULT_SKIP_LOAD = 5
 NVFP4_OPT_PREFETCH_STAGES = 6
 NVFP4_OPT_SPLIT_TAIL = 7
 NVFP4_OPT_CTA_PAIR = 8
+NVFP4_OPT_SF_DIRECT = 9
 
 
 class Nvfp4Error(RuntimeError):
@@ -82,6 +84,8 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_last_cuda_error.argtypes = []
     lib.nvfp4_last_kernel.restype = ctypes.c_char_p
     lib.nvfp4_last_kernel.argtypes = []
+    lib.nvfp4_last_launches.restype = ctypes.c_int
+    lib.nvfp4_last_launches.argtypes = []
     lib.nvfp4_set_option.restype = ctypes.c_int
     lib.nvfp4_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.nvfp4_release.restype = None
@@ -159,6 +163,10 @@ def nvfp4_last_cuda_error() -> int:
 
 def nvfp4_last_kernel() -> str:
     return _get().nvfp4_last_kernel().decode()
+
+
+def nvfp4_last_launches() -> int:
+    return _get().nvfp4_last_launches()
 
 
 def nvfp4_set_option(option: int, value: int) -> None:

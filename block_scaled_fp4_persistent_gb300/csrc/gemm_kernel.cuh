@@ -13,7 +13,10 @@
 //   warps 2-5   scale stagers. Per stage each warp reads its rows of the scale
 //               blocks from shared memory and writes them into the stage's TMEM
 //               scale slot with tcgen05.st, in the layout that
-//               tcgen05.cp .32x128b.warpx4 would produce.
+//               tcgen05.cp .32x128b.warpx4 would produce. The scales arrive either
+//               as prepacked 512-byte atoms (bulk copies) or as row-major rows of
+//               16 bytes per stage (TMA tensor copies); the stagers transpose the
+//               latter on the way, so row-major scales need no separate pass.
 //   warps 6-13  epilogue. Two warps per TMEM lane quarter, each owning BN/2
 //               columns. They drain the accumulator 32 columns at a time, convert to
 //               fp16, and send each 32 x 32 block out through a swizzled shared-memory
@@ -60,6 +63,7 @@ constexpr int kBlockM = 128;
 constexpr int kBlockK = 256;             // K per stage = 128 bytes of E2M1 per row
 constexpr int kRowBytes = kBlockK / 2;   // 128
 constexpr int kScaleBlockBytes = 512;    // scales of 128 rows x 64 K
+constexpr int kSfRowBytes = kBlockK / 16;  // one row's scales of one K-stage in the row-major layout: 16
 constexpr uint32_t kTmemCols = 512;
 constexpr int kEpiBufBytes = 32 * 64;    // one epilogue staging buffer: 32 rows x 64 bytes
 
@@ -100,6 +104,77 @@ struct Layout {
 // Item `it` of the table. Read through the items pointer passed with the launch, it
 // is one load: through the table header's offset it would be two dependent ones,
 // each a DRAM round trip at the start of a launch.
+// A stager lane's view of one 128-row region of a stage's scales: the four 16-byte
+// rows at base + 512 t (t = 0..3), base including the lane's 16-byte offset. The
+// word the MMA wants for K-block j and row lane + 32 i is word i of row t = j in
+// the blocked layout (atom j, the 4 scales of rows lane, lane + 32, ...), and word j
+// of row t = i in the row-major layout (row lane + 32 i's 16 scales of the stage,
+// 4 per K-block): the same four loads, transposed.
+struct ScaleRows {
+    uint4 q[4];
+    __device__ __forceinline__ void load(const uint8_t *base)
+    {
+#pragma unroll
+        for (int t = 0; t < 4; ++t)
+            q[t] = *reinterpret_cast<const uint4 *>(base + t * kScaleBlockBytes);
+    }
+    static __device__ __forceinline__ uint32_t part(const uint4 &v, int c)
+    {
+        return c == 0 ? v.x : c == 1 ? v.y : c == 2 ? v.z : v.w;
+    }
+    template <bool kRowMajor>
+    __device__ __forceinline__ uint32_t word(int j, int i) const
+    {
+        return kRowMajor ? part(q[i], j) : part(q[j], i);
+    }
+};
+
+// One stager warp's part of one stage: SFA (one 128-row region at src) to TMEM
+// columns col .. col+15, then SFB (kHalves regions after kSfaBytes) to columns
+// col + kSfbCol ..., 16 per store, in the order (K-block j, half h, word i).
+template <bool kRowMajor, int kHalves>
+__device__ __forceinline__ void stage_scales(const uint8_t *src, int sfa_bytes, uint32_t col, uint32_t sfb_col)
+{
+    ScaleRows a;
+    a.load(src);
+    uint32_t ra[16];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+            ra[4 * j + i] = a.word<kRowMajor>(j, i);
+    tmem_store_16cols(col, ra);
+    ScaleRows b[kHalves];
+#pragma unroll
+    for (int h = 0; h < kHalves; ++h)
+        b[h].load(src + sfa_bytes + h * 4 * kScaleBlockBytes);
+#pragma unroll
+    for (int batch = 0; batch < kHalves; ++batch) {
+        uint32_t rb[16];
+#pragma unroll
+        for (int x = 0; x < 4; ++x) {
+            const int idx = batch * 4 + x;  // 0 .. 4*kHalves-1: the (j, h) block in column order
+            const int j = idx / kHalves, h = idx % kHalves;
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                rb[4 * x + i] = b[h].word<kRowMajor>(j, i);
+        }
+        tmem_store_16cols(col + sfb_col + 16 * batch, rb);
+    }
+}
+
+// Prefetches the scale tensor maps of the groups whose scales are row-major, by
+// the lanes of one warp that has nothing else to do at start-up (each lane reads
+// its group's flag first).
+__device__ __forceinline__ void prefetch_scale_maps(const Table *tab, int num_groups, uint32_t lane)
+{
+    for (int i = (int)lane; i < 2 * min(num_groups, 64); i += 32) {
+        const GroupEntry &g = tab->group(i / 2);
+        if (g.sf_rowmajor)
+            tensormap_prefetch(i % 2 == 0 ? &g.tmap_sfa : &g.tmap_sfb);
+    }
+}
+
 __device__ __forceinline__ WorkItem global_item(const KernelArgs &args, uint32_t it)
 {
     const int4 *p = args.items + 4 * (size_t)it;
@@ -253,8 +328,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
         first_item = global_item(args, item_begin);
-    // The groups' tensor maps, fetched ahead by the producer warp's lanes in
-    // parallel: one prefetch.tensormap per lane.
+    // The groups' operand tensor maps, fetched ahead by the producer warp's lanes
+    // in parallel: one prefetch.tensormap per lane.
     if (warp == kProducerWarp)
         for (int i = (int)lane; i < 2 * min(args.num_groups, 64); i += 32) {
             const GroupEntry &g = tab->group(i / 2);
@@ -306,7 +381,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 int32_t ya, yb;
                 int kb64, kb_begin, kb_end;
                 bool b_shared;
-                const uint8_t *sfa;
+                bool sf_rowmajor;              // scales through tmap_sfa / tmap_sfb at rows ya / yb
+                const void *tmap_sfa, *tmap_sfb;
+                const uint8_t *sfa;            // else blocked scale atoms
                 const uint8_t *sfb[L::kHalves];
             };
             // Everything but the tensor maps' addresses comes from the item itself.
@@ -322,6 +399,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 r.kb_begin = w.kb_begin;
                 r.kb_end = w.kb_end;
                 r.b_shared = (w.flags & kItemBShared) != 0;
+                r.sf_rowmajor = (w.flags & kItemSfRowMajor) != 0;
+                r.tmap_sfa = &ge.tmap_sfa;
+                r.tmap_sfb = &ge.tmap_sfb;
                 r.sfa = w.sfa;
                 // The scales of B come in 128-row tiles. A half of the B tile that lies
                 // wholly past N reads the first half's scales instead: its B rows are
@@ -342,10 +422,15 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     const uint32_t sfb_bytes = (uint32_t)min(4, pf.kb64 - pf_kb * 4) * kScaleBlockBytes;
                     tma_prefetch_2d(pf.tmap_a, pf_kb * kRowBytes, pf.ya);
                     tma_prefetch_2d(pf.tmap_b, pf_kb * kRowBytes, pf.yb);
-                    bulk_prefetch(pf.sfa + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
+                    if (pf.sf_rowmajor) {
+                        tma_prefetch_2d(pf.tmap_sfa, pf_kb * kSfRowBytes, pf.ya);
+                        tma_prefetch_2d(pf.tmap_sfb, pf_kb * kSfRowBytes, pf.yb);
+                    } else {
+                        bulk_prefetch(pf.sfa + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
 #pragma unroll
-                    for (int h = 0; h < L::kHalves; ++h)
-                        bulk_prefetch(pf.sfb[h] + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
+                        for (int h = 0; h < L::kHalves; ++h)
+                            bulk_prefetch(pf.sfb[h] + (size_t)pf_kb * 4 * kScaleBlockBytes, sfb_bytes);
+                    }
                     ++pf_g;
                     if (++pf_kb == pf.kb_end) {
                         if (++pf_it < item_end) {
@@ -377,11 +462,16 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     if (!(args.fault_skip_load >= 0 && blockIdx.x == 0 && kiter == (uint32_t)args.fault_skip_load)) {
                         tma_load_2d(slot, src.tmap_a, kb * kRowBytes, src.ya, fb, pol_a);
                         tma_load_2d(slot + L::kOffB, src.tmap_b, kb * kRowBytes, src.yb, fb, pol_b);
-                        bulk_load(slot + L::kOffSfa, src.sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
+                        if (src.sf_rowmajor) {  // K % 256 == 0: always a whole stage (sf_bytes = 2 KB)
+                            tma_load_2d(slot + L::kOffSfa, src.tmap_sfa, kb * kSfRowBytes, src.ya, fb, pol_a);
+                            tma_load_2d(slot + L::kOffSfb, src.tmap_sfb, kb * kSfRowBytes, src.yb, fb, pol_b);
+                        } else {
+                            bulk_load(slot + L::kOffSfa, src.sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
 #pragma unroll
-                        for (int h = 0; h < L::kHalves; ++h)
-                            bulk_load(slot + L::kOffSfb + h * 4 * kScaleBlockBytes,
-                                      src.sfb[h] + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_b);
+                            for (int h = 0; h < L::kHalves; ++h)
+                                bulk_load(slot + L::kOffSfb + h * 4 * kScaleBlockBytes,
+                                          src.sfb[h] + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_b);
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -468,10 +558,11 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         }
     } else if (warp < kEpilogueWarp0) {
         // ------------------------------------------------------ scale stagers
-        // Lane r of the warp for TMEM lane quarter q writes TMEM lane 32q + r. Word c of
-        // a 512-byte block's row r holds the 4 k-scales of row r + 32c; it goes to the
-        // block's column base + c. That is the layout tcgen05.cp .32x128b.warpx4
-        // produces, repeated in all four quarters.
+        // Lane r of the warp for TMEM lane quarter q writes TMEM lane 32q + r. The 4
+        // k-scales of row r + 32c for K-block j go to column base(j) + c (see
+        // ScaleRows for where they sit in shared memory, blocked or row-major). That
+        // is the layout tcgen05.cp .32x128b.warpx4 produces, repeated in all four
+        // quarters.
         const int quarter = warp % 4;  // warps 2,3,4,5 -> quarters 2,3,0,1
         const uint32_t lane_off = (uint32_t)(quarter * 32) << 16;
         uint32_t stage = 0, phase = 0;
@@ -485,27 +576,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 }
                 const uint8_t *src = ring + stage * L::kStageBytes + L::kOffSfa + lane * 16;
                 const uint32_t col = tmem_sf + lane_off + stage * L::kSfColsPerStage;
-                uint32_t ra[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(src + j * kScaleBlockBytes);
-                    ra[4 * j + 0] = a.x, ra[4 * j + 1] = a.y, ra[4 * j + 2] = a.z, ra[4 * j + 3] = a.w;
-                }
-                tmem_store_16cols(col, ra);
-                // SFB: columns in order (k-block j, half h, word c), 16 per store
-#pragma unroll
-                for (int batch = 0; batch < L::kHalves; ++batch) {
-                    uint32_t rb[16];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int idx = batch * 4 + x;  // 0 .. 4*kHalves-1: the (j, h) block in column order
-                        const int j = idx / L::kHalves, h = idx % L::kHalves;
-                        const uint4 b = *reinterpret_cast<const uint4 *>(src + L::kSfaBytes +
-                                                                         (h * 4 + j) * kScaleBlockBytes);
-                        rb[4 * x + 0] = b.x, rb[4 * x + 1] = b.y, rb[4 * x + 2] = b.z, rb[4 * x + 3] = b.w;
-                    }
-                    tmem_store_16cols(col + L::kSfbCol + 16 * batch, rb);
-                }
+                if (w.flags & kItemSfRowMajor)
+                    stage_scales<true, L::kHalves>(src, L::kSfaBytes, col, L::kSfbCol);
+                else
+                    stage_scales<false, L::kHalves>(src, L::kSfaBytes, col, L::kSfbCol);
                 tmem_store_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -528,6 +602,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         constexpr int kCols = BN / 2;
         const uint32_t t_addr = tmem_base + ((uint32_t)(quarter * 32) << 16) + chalf * kCols;
         EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
+        if (warp == kEpilogueWarp0)
+            prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);

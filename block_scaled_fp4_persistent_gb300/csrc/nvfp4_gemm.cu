@@ -40,6 +40,7 @@ namespace {
 
 std::atomic<int> g_last_cuda_error{0};
 std::atomic<const char *> g_last_kernel{"none"};  // the variant the last call launched
+std::atomic<int> g_last_launches{0};  // kernels the last GEMM call launched (prepack and GEMM)
 
 struct Options {
     std::atomic<int64_t> block_n{0};
@@ -50,6 +51,7 @@ struct Options {
     std::atomic<int64_t> prefetch_stages{-1};  // -1 = automatic
     std::atomic<int64_t> split_tail{1};  // 0 off, 1 single CTAs only, 2 single CTAs and pairs
     std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
+    std::atomic<int64_t> sf_direct{1};  // 1 = row-major scales read by the GEMM kernel where K % 256 == 0
 } g_opt;
 
 constexpr int kMaxDevices = 64;
@@ -195,6 +197,27 @@ int encode_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, u
     return NVFP4_OK;
 }
 
+// Row-major scales [rows][K/16] read as boxes of 16 bytes (one 256-K stage) x
+// box_rows, unswizzled: a box lands as box_rows rows of 16 bytes. Rows past the
+// matrix read as zero. Without scales to read (prepacked groups), a valid map of the
+// buffer's first 16 bytes, which the kernel never copies through.
+int encode_scale_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
+{
+    cuuint64_t dims[2] = {row_bytes, rows};
+    cuuint64_t strides[1] = {row_bytes};
+    cuuint32_t box[2] = {16, box_rows};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void *>(base), dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error.store(10000 + (int)r);
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+int encode_unused_scale_map(CUtensorMap *map, const void *base) { return encode_scale_map(map, base, 16, 1, 1); }
+
 // The fp16 output [M][N] as 32 x 32 boxes (64 bytes per box row) with the
 // 64-byte swizzle, for TMA stores from the epilogue's staging buffers.
 int encode_output_map(CUtensorMap *map, void *C, uint64_t M, uint64_t N)
@@ -238,7 +261,8 @@ int check_problem(const Nvfp4Problem &p)
 
 // One active group as the table sees it (scale pointers already blocked).
 struct ActiveGroup {
-    int32_t M, N, K, pad;
+    int32_t M, N, K;
+    int32_t sf_rowmajor;  // 1: the kernel reads row-major scales through tensor maps
     const void *A, *B, *SFA, *SFB;
     void *C;
 };
@@ -274,7 +298,7 @@ WorkItem make_item(const ActiveGroup &g, int group, int m, int n, int kb_begin, 
     const int ra = m * (block_m / 128), rb = n * (block_n / 128);
     w.flags = ((g.M + block_m - 1) / block_m > 1 ? kItemBShared : 0) |
               (block_m == 256 && ra + 1 < row_tiles_a ? kItemA2 : 0) |
-              (block_n == 256 && rb + 1 < row_tiles_b ? kItemB2 : 0);
+              (block_n == 256 && rb + 1 < row_tiles_b ? kItemB2 : 0) | (g.sf_rowmajor ? kItemSfRowMajor : 0);
     const size_t blocks = (size_t)kb64 * kScaleBlockBytes;
     w.sfa = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFA) + (size_t)ra * blocks);
     w.sfb = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFB) + (size_t)rb * blocks);
@@ -505,6 +529,13 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
             rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, pair ? 128u : (uint32_t)block_n);
         if (!rc)
             rc = encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
+        if (!rc)
+            rc = a.sf_rowmajor ? encode_scale_map(&e.tmap_sfa, a.SFA, (uint64_t)a.K / 16, (uint64_t)a.M, kBlockM)
+                               : encode_unused_scale_map(&e.tmap_sfa, a.SFA);
+        if (!rc)
+            rc = a.sf_rowmajor ? encode_scale_map(&e.tmap_sfb, a.SFB, (uint64_t)a.K / 16, (uint64_t)a.N,
+                                                  pair ? (uint32_t)kPairBlockN : (uint32_t)block_n)
+                               : encode_unused_scale_map(&e.tmap_sfb, a.SFB);
         if (rc) {
             cudaFreeHost(t.host);
             return rc;
@@ -518,6 +549,7 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         e.kblocks64 = a.K / 64;
         e.tiles_m = (a.M + block_m - 1) / block_m;
         e.tiles_n = (a.N + block_n - 1) / block_n;
+        e.sf_rowmajor = a.sf_rowmajor;
     }
     memcpy(h + off_cta, cta_begin.data(), cta_begin.size() * sizeof(uint32_t));
     if (!items.empty())
@@ -705,7 +737,9 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
             CUDA_TRY(cudaMemsetAsync(p.C, 0, (size_t)p.M * p.N * sizeof(__half), stream));
     }
 
-    // Row-major scales go through the prepack kernel into this stream's workspace.
+    // Row-major scales are read directly by the kernel where their rows are whole
+    // multiples of 16 bytes (K % 256 == 0); the others go through the prepack kernel
+    // into this stream's workspace.
     std::vector<ActiveGroup> gs;
     std::vector<PrepackJob> jobs;
     size_t ws_bytes = 0;
@@ -714,8 +748,9 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         const Nvfp4Problem &p = probs[i];
         if (p.M == 0 || p.N == 0 || p.K == 0)
             continue;
-        gs.push_back(ActiveGroup{p.M, p.N, p.K, 0, p.A, p.B, p.SFA, p.SFB, p.C});
-        if (p.sf_layout == NVFP4_SF_ROWMAJOR) {
+        const bool direct = p.sf_layout == NVFP4_SF_ROWMAJOR && g_opt.sf_direct.load() != 0 && p.K % 256 == 0;
+        gs.push_back(ActiveGroup{p.M, p.N, p.K, direct ? 1 : 0, p.A, p.B, p.SFA, p.SFB, p.C});
+        if (p.sf_layout == NVFP4_SF_ROWMAJOR && !direct) {
             const size_t oa = ws_bytes;
             ws_bytes += (blocked_scale_bytes(p.M, p.K / 16) + 255) & ~size_t(255);
             const size_t ob = ws_bytes;
@@ -743,6 +778,7 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         }
         CUDA_TRY(launch_prepack(jobs.data(), (int)jobs.size(), stream));
     }
+    const int prepack_launches = jobs.empty() ? 0 : 1;
 
     // BLOCK_N or STAGES select a single-CTA variant; CTA_PAIR forces either kind.
     const int64_t opt_pair = g_opt.cta_pair.load();
@@ -768,12 +804,15 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     if (rc)
         return rc;
     switch (variant) {
-    case 0: return launch_gemm<128, kDeepStages128>(*ds, *t, stream, (int)gs.size());
-    case 1: return launch_gemm<128, 2>(*ds, *t, stream, (int)gs.size());
-    case 2: return launch_gemm<256, kDeepStages256>(*ds, *t, stream, (int)gs.size());
-    case 3: return launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size());
-    default: return launch_pair(*ds, *t, stream, (int)gs.size());
+    case 0: rc = launch_gemm<128, kDeepStages128>(*ds, *t, stream, (int)gs.size()); break;
+    case 1: rc = launch_gemm<128, 2>(*ds, *t, stream, (int)gs.size()); break;
+    case 2: rc = launch_gemm<256, kDeepStages256>(*ds, *t, stream, (int)gs.size()); break;
+    case 3: rc = launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size()); break;
+    default: rc = launch_pair(*ds, *t, stream, (int)gs.size()); break;
     }
+    if (rc == NVFP4_OK)
+        g_last_launches.store(prepack_launches + 1);
+    return rc;
 }
 
 extern "C" size_t nvfp4_prepacked_scale_bytes(int rows, int K)
@@ -853,6 +892,8 @@ extern "C" int nvfp4_last_cuda_error(void) { return g_last_cuda_error.load(); }
 
 extern "C" const char *nvfp4_last_kernel(void) { return g_last_kernel.load(); }
 
+extern "C" int nvfp4_last_launches(void) { return g_last_launches.load(); }
+
 extern "C" int nvfp4_set_option(int option, int64_t value)
 {
     switch (option) {
@@ -880,6 +921,11 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         if (value < 0 || value > 2)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.split_tail = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_SF_DIRECT:
+        if (value < 0 || value > 1)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.sf_direct = value;
         return NVFP4_OK;
     case NVFP4_OPT_CTA_PAIR:
         if (value < 0 || value > 2)
@@ -954,10 +1000,11 @@ extern "C" void nvfp4_release(void)
 // Limits and rules (repeated in the header):
 //  * Scratch size kNoAllocScratchBytes (256 KB). The first 256 bytes hold the
 //    error words and the rest holds the table:
-//    128 + sizeof(GroupEntry) * g + 4 * (grid + 1) (rounded up to 16) + 16 * tiles,
+//    128 + sizeof(GroupEntry) * g + 4 * (grid + 1) (rounded up to 16) + 64 * tiles,
 //    where tiles = sum over groups of ceil(M/128) * ceil(N/128). A larger
 //    problem set returns NVFP4_ERR_TOO_LARGE and launches nothing.
-//  * Only NVFP4_SF_PREPACKED scales. The row-major path would need a workspace.
+//  * Row-major scales only where K % 256 == 0, read directly by the kernel: the
+//    prepack pass would need a workspace.
 //  * All calls share the one array. A call overwrites the previous call's table
 //    in stream order. Calls that can overlap on the GPU (on different streams,
 //    without ordering between them) race on it and must not be issued.
@@ -1028,7 +1075,9 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     for (int i = 0; i < g; ++i) {
         if (int rc = check_problem(probs[i]))
             return rc;
-        if (probs[i].sf_layout != NVFP4_SF_PREPACKED)
+        // row-major scales only where the kernel reads them directly (no workspace here)
+        const Nvfp4Problem &p = probs[i];
+        if (p.sf_layout == NVFP4_SF_ROWMAJOR && p.M > 0 && p.N > 0 && p.K > 0 && p.K % 256 != 0)
             return NVFP4_ERR_INVALID_ARG;
     }
 
@@ -1109,6 +1158,13 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
             rc = encode_operand_map(&e.tmap_b, p.B, (uint64_t)p.K / 2, (uint64_t)p.N, (uint32_t)BN);
         if (!rc)
             rc = encode_output_map(&e.tmap_c, p.C, (uint64_t)p.M, (uint64_t)p.N);
+        const bool rm = p.sf_layout == NVFP4_SF_ROWMAJOR;
+        if (!rc)
+            rc = rm ? encode_scale_map(&e.tmap_sfa, p.SFA, (uint64_t)p.K / 16, (uint64_t)p.M, kBlockM)
+                    : encode_unused_scale_map(&e.tmap_sfa, p.SFA);
+        if (!rc)
+            rc = rm ? encode_scale_map(&e.tmap_sfb, p.SFB, (uint64_t)p.K / 16, (uint64_t)p.N, (uint32_t)BN)
+                    : encode_unused_scale_map(&e.tmap_sfb, p.SFB);
         if (rc)
             return rc;
         e.sfa = static_cast<const uint8_t *>(p.SFA);
@@ -1120,7 +1176,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         e.kblocks64 = p.K / 64;
         e.tiles_m = (p.M + kBlockM - 1) / kBlockM;
         e.tiles_n = (p.N + BN - 1) / BN;
-        const ActiveGroup a{p.M, p.N, p.K, 0, p.A, p.B, p.SFA, p.SFB, p.C};
+        e.sf_rowmajor = rm ? 1 : 0;
+        const ActiveGroup a{p.M, p.N, p.K, rm ? 1 : 0, p.A, p.B, p.SFA, p.SFB, p.C};
         for (int n = 0; n < e.tiles_n; ++n)
             for (int m = 0; m < e.tiles_m; ++m, ++t)
                 items[cta_begin[list_of_tile(t, grid)] + t / ((size_t)kPipes * grid)] =
@@ -1150,5 +1207,6 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
     CUDA_TRY(cudaGetLastError());
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");
+    g_last_launches.store(1);
     return NVFP4_OK;
 }

@@ -167,6 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const uint8_t *sfa = w.sfa + ((rank == 1 && (w.flags & kItemA2)) ? half : 0);
                 const uint8_t *sfb[2] = {w.sfb, w.sfb + ((w.flags & kItemB2) ? half : 0)};
                 const uint64_t pol_b = (w.flags & kItemBShared) ? pol_b_shared : pol_b_stream;
+                const bool sf_rm = (w.flags & kItemSfRowMajor) != 0;
                 for (int kb = w.kb_begin; kb < w.kb_end; ++kb, ++kiter) {
                     if (!wait_phase(smem_addr(&empty[stage]), phase ^ 1u, sh, args, kRoleProducer, (int)it, kb)) {
                         ok = false;
@@ -181,11 +182,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     if (!(args.fault_skip_load >= 0 && blockIdx.x == 0 && kiter == (uint32_t)args.fault_skip_load)) {
                         tma_load_2d(slot, &ge.tmap_a, kb * kRowBytes, ya, fb, pol_a);
                         tma_load_2d(slot + L::kOffB, &ge.tmap_b, kb * kRowBytes, yb, fb, pol_b);
-                        bulk_load(slot + L::kOffSfa, sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
+                        if (sf_rm) {  // K % 256 == 0: a whole stage; B's box is both halves, 256 rows
+                            tma_load_2d(slot + L::kOffSfa, &ge.tmap_sfa, kb * kSfRowBytes, ya, fb, pol_a);
+                            tma_load_2d(slot + L::kOffSfb, &ge.tmap_sfb, kb * kSfRowBytes, w.tile_n * kPairBlockN, fb,
+                                        pol_b);
+                        } else {
+                            bulk_load(slot + L::kOffSfa, sfa + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_a);
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-                            bulk_load(slot + L::kOffSfb + h * 4 * kScaleBlockBytes, sfb[h] + (size_t)kb * 4 * kScaleBlockBytes,
-                                      sf_bytes, fb, pol_b);
+                            for (int h = 0; h < 2; ++h)
+                                bulk_load(slot + L::kOffSfb + h * 4 * kScaleBlockBytes,
+                                          sfb[h] + (size_t)kb * 4 * kScaleBlockBytes, sf_bytes, fb, pol_b);
+                        }
                     }
                     if (++stage == STAGES) {
                         stage = 0;
@@ -279,25 +286,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 }
                 const uint8_t *src = ring + stage * L::kStageBytes + L::kOffSfa + lane * 16;
                 const uint32_t col = tmem_sf + lane_off + stage * L::kSfColsPerStage;
-                uint32_t ra[16];
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const uint4 a = *reinterpret_cast<const uint4 *>(src + j * kScaleBlockBytes);
-                    ra[4 * j + 0] = a.x, ra[4 * j + 1] = a.y, ra[4 * j + 2] = a.z, ra[4 * j + 3] = a.w;
-                }
-                tmem_store_16cols(col, ra);
-#pragma unroll
-                for (int batch = 0; batch < 2; ++batch) {
-                    uint32_t rb[16];
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int idx = batch * 4 + x;  // (k-block j, half h) in column order
-                        const int j = idx / 2, h = idx % 2;
-                        const uint4 b = *reinterpret_cast<const uint4 *>(src + L::kSfaBytes + (h * 4 + j) * kScaleBlockBytes);
-                        rb[4 * x + 0] = b.x, rb[4 * x + 1] = b.y, rb[4 * x + 2] = b.z, rb[4 * x + 3] = b.w;
-                    }
-                    tmem_store_16cols(col + L::kSfbCol + 16 * batch, rb);
-                }
+                if (w.flags & kItemSfRowMajor)
+                    stage_scales<true, 2>(src, L::kSfaBytes, col, L::kSfbCol);
+                else
+                    stage_scales<false, 2>(src, L::kSfaBytes, col, L::kSfbCol);
                 tmem_store_wait();
                 tc_fence_before();
                 __syncwarp();
@@ -332,6 +324,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         };
         // C goes out through this warp's two staging buffers and TMA stores
         EpilogueStager out{smem + L::kOffEpi + (warp - kEpilogueWarp0) * 2 * kEpiBufBytes};
+        if (warp == kEpilogueWarp0)
+            prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);

@@ -21,13 +21,19 @@ constexpr int kStatusTimeout = -5;  // NVFP4_ERR_TIMEOUT
 struct alignas(128) GroupEntry {
     CUtensorMap tmap_a;   // uint8 [M][K/2], box 128 B x 128 rows, 128-byte swizzle
     CUtensorMap tmap_b;   // uint8 [N][K/2], box 128 B x BLOCK_N rows, 128-byte swizzle
-    CUtensorMap tmap_c;   // fp16 [M][N], box 32 x 32, 64-byte swizzle (CTA-pair kernel's stores)
-    const uint8_t *sfa;   // blocked scales of A: ceil(M/128) x kblocks64 blocks of 512 B
-    const uint8_t *sfb;   // blocked scales of B: ceil(N/128) x kblocks64 blocks of 512 B
+    CUtensorMap tmap_c;   // fp16 [M][N], box 32 x 32, 64-byte swizzle (the epilogues' stores)
+    // Row-major scales (kItemSfRowMajor): uint8 [M][K/16] and [N][K/16], boxes of 16 B
+    // (one K-stage) x 128 rows (A) and x the tile's B rows, no swizzle. For prepacked
+    // scales, valid but unused maps of the scale buffers' first 16 bytes.
+    CUtensorMap tmap_sfa;
+    CUtensorMap tmap_sfb;
+    const uint8_t *sfa;   // scales of A: blocked, ceil(M/128) x kblocks64 blocks of 512 B, or row-major
+    const uint8_t *sfb;   // scales of B: the same
     __half *C;            // [M][N] fp16
     int32_t M, N, K;
     int32_t kblocks64;    // K / 64
     int32_t tiles_m, tiles_n;
+    int32_t sf_rowmajor;  // 1: the scales are row-major, read through tmap_sfa / tmap_sfb
 };
 
 // One segment of an output tile: K-stages kb_begin .. kb_end-1 (256 K each).
@@ -53,7 +59,7 @@ struct WorkItem {
     int32_t nseg;
     int32_t ws_slot;
     int32_t kblocks64;
-    int32_t flags;  // kItemBShared | kItemA2 | kItemB2
+    int32_t flags;  // kItemBShared | kItemA2 | kItemB2 | kItemSfRowMajor
     int32_t reserved;
     const uint8_t *sfa;  // scale blocks of the tile's first 128 A rows (kblocks64 blocks of 512 B)
     const uint8_t *sfb;  // scale blocks of the tile's first 128 B rows
@@ -62,6 +68,7 @@ struct WorkItem {
 constexpr int32_t kItemBShared = 1;  // the group has several m-tiles: its B tiles are read more than once
 constexpr int32_t kItemA2 = 2;       // rows 128..255 of the tile's A rows exist (their scales follow sfa)
 constexpr int32_t kItemB2 = 4;       // rows 128..255 of the tile's B rows exist (their scales follow sfb)
+constexpr int32_t kItemSfRowMajor = 8;  // the group's scales are row-major, read through tmap_sfa / tmap_sfb
 
 static_assert(sizeof(WorkItem) == 64, "WorkItem is read as four int4");
 

@@ -55,7 +55,11 @@ enum {
     /* The 128 x 4 blocked layout: see nvfp4_prepack_scales(). This is the layout
      * the kernel reads. */
     NVFP4_SF_PREPACKED = 0,
-    /* Row-major [rows][K/16]. The call first runs the prepack kernel into a
+    /* Row-major [rows][K/16]. Where K % 256 == 0 (rows of K/16 bytes, a multiple of
+     * 16) the GEMM kernel reads them directly: each K-stage's 16 scale bytes per row
+     * arrive by TMA and the kernel rearranges them on their way into tensor memory,
+     * so the call is one launch, as fast as with prepacked scales. Otherwise (or with
+     * NVFP4_OPT_SF_DIRECT 0) the call first runs the prepack kernel into a
      * library-owned workspace (one extra launch), then the GEMM. */
     NVFP4_SF_ROWMAJOR = 1
 };
@@ -137,6 +141,11 @@ int nvfp4_last_cuda_error(void);
  * string: the caller does not free it. */
 const char *nvfp4_last_kernel(void);
 
+/* How many kernels the last successful GEMM call of this process launched: 1
+ * (the GEMM), or 2 when row-major scales first went through the prepack kernel;
+ * 0 before the first launch. */
+int nvfp4_last_launches(void);
+
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
  *  NVFP4_OPT_CTA_PAIR      : 0 = automatic, 1 = CTA pairs, 2 = single CTAs.
@@ -169,6 +178,9 @@ const char *nvfp4_last_kernel(void);
  *                             the busiest CTA's work.
  *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
  *                             (default 2,000,000 us)
+ *  NVFP4_OPT_SF_DIRECT     : 1 = row-major scales are read directly by the GEMM
+ *                             kernel where K % 256 == 0 (default), 0 = always
+ *                             prepacked by an extra launch first
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
  *                             CTA 0 skips the copies of its k-stage with that
  *                             global index. The consumer's wait then runs out
@@ -183,7 +195,8 @@ enum {
     NVFP4_OPT_FAULT_SKIP_LOAD = 5,
     NVFP4_OPT_PREFETCH_STAGES = 6,
     NVFP4_OPT_SPLIT_TAIL = 7,
-    NVFP4_OPT_CTA_PAIR = 8
+    NVFP4_OPT_CTA_PAIR = 8,
+    NVFP4_OPT_SF_DIRECT = 9
 };
 int nvfp4_set_option(int option, int64_t value);
 
@@ -205,12 +218,13 @@ void nvfp4_release(void);
  * array until the process exits.
  *
  * Same arguments and results as nvfp4_grouped_gemm, with these limits:
- *  - Scales must be NVFP4_SF_PREPACKED. Otherwise NVFP4_ERR_INVALID_ARG.
+ *  - Scales NVFP4_SF_PREPACKED, or NVFP4_SF_ROWMAJOR where K % 256 == 0 (read
+ *    directly by the kernel). Row-major scales with another K: NVFP4_ERR_INVALID_ARG.
  *  - The problem table must fit the array:
- *      128 + 384*g' + 4*(grid+1) (rounded up to 16) + 16*tiles <= 262144 - 256 bytes,
+ *      128 + 640*g' + 4*(grid+1) (rounded up to 16) + 64*tiles <= 262144 - 256 bytes,
  *    where g' counts the groups with M, N, K > 0,
  *    tiles = sum ceil(M/128)*ceil(N/128) and grid = min(tiles, SM count).
- *    In practice that is up to about 16,000 tiles of 128 x 128 for a few
+ *    In practice that is up to about 4,000 tiles of 128 x 128 for a few
  *    groups. A larger set returns NVFP4_ERR_TOO_LARGE and launches nothing.
  *  - Every call shares the one array. A call rewrites the table in stream
  *    order, and a kernel that is still running on another stream would read

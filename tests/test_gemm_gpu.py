@@ -27,7 +27,7 @@ def _defaults():
     yield
     for opt, val in [(nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_BLOCK_N, 0),
                      (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
-                     (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0)]:
+                     (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0), (nv.NVFP4_OPT_SF_DIRECT, 1)]:
         nv.nvfp4_set_option(opt, val)
 
 
@@ -81,12 +81,41 @@ RAGGED = dict(seed=77, Ms=[1, 40, 127, 128, 129, 248, 300], Ns=[8, 120, 136, 512
 @pytest.mark.parametrize("layout", [nv.NVFP4_SF_PREPACKED, nv.NVFP4_SF_ROWMAJOR])
 def test_ragged_shapes_one_launch(layout, pair):
     # CTA pairs: M = 1..300 leaves the second CTA's rows partly or wholly past M, and
-    # N = 8..264 leaves the second half of the B tile partly or wholly past N
+    # N = 8..264 leaves the second half of the B tile partly or wholly past N. With
+    # row-major scales the groups with K % 256 == 0 read them in the kernel and the
+    # others through the prepack kernel, in the same call.
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_problem_set(RAGGED["seed"], RAGGED["Ms"], RAGGED["Ns"], RAGGED["Ks"])
     d = [DeviceGroup(g, layout) for g in groups]
     run(d)
+    assert nv.nvfp4_last_launches() == (2 if layout == nv.NVFP4_SF_ROWMAJOR else 1)
     check_full(groups, d, f"ragged layout={layout} pair={pair}")
+
+
+# K % 256 == 0 throughout: every group reads its row-major scales in the kernel
+DIRECT = dict(seed=78, Ms=[1, 40, 127, 129, 248, 300], Ns=[8, 136, 512, 264, 128, 72],
+              Ks=[256, 512, 768, 1024, 2304, 256])
+
+
+@pytest.mark.parametrize("pair,block_n", [(1, 0), (2, 0), (2, 256)])
+def test_row_major_scales_read_in_the_kernel(pair, block_n):
+    # one launch, and the same bits as prepacked scales and as the prepack route
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, block_n)
+    groups = gen.make_problem_set(DIRECT["seed"], DIRECT["Ms"], DIRECT["Ns"], DIRECT["Ks"])
+    d = [DeviceGroup(g, nv.NVFP4_SF_ROWMAJOR) for g in groups]
+    run(d)
+    assert nv.nvfp4_last_launches() == 1
+    check_full(groups, d, f"row-major in the kernel pair={pair} block_n={block_n}")
+    pre = [DeviceGroup(g) for g in groups]
+    run(pre)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, 0)
+    via = [DeviceGroup(g, nv.NVFP4_SF_ROWMAJOR) for g in groups]
+    run(via)
+    assert nv.nvfp4_last_launches() == 2
+    for a, b, c in zip(d, pre, via):
+        assert np.array_equal(a.result().view(np.uint16), b.result().view(np.uint16))
+        assert np.array_equal(a.result().view(np.uint16), c.result().view(np.uint16))
 
 
 def test_structured_closed_form():
@@ -199,10 +228,12 @@ def sample_indices(M, N, n, rng):
 @pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
 def test_full_size_workloads_sampled(name, pair):
     # pair 0: the automatic choice, the benchmark's launch configuration; 1: CTA pairs;
-    # 2: single CTAs
+    # 2: single CTAs. Pairs read row-major scales in the kernel (the e2e benchmark's
+    # route), the others prepacked ones.
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_workload(name)
-    d = [DeviceGroup(g) for g in groups]
+    layout = nv.NVFP4_SF_ROWMAJOR if pair == 1 else nv.NVFP4_SF_PREPACKED
+    d = [DeviceGroup(g, layout) for g in groups]
     run(d)  # default options: the launch configuration of the benchmark
     rng = np.random.default_rng(99)
     again = None

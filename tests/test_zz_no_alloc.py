@@ -62,5 +62,31 @@ def test_noalloc_rejects_what_it_cannot_hold():
     # 16384 x 16384 output tiles' worth of table: far beyond the fixed array; nothing is launched
     big = nv.Nvfp4Problem(1 << 21, 1 << 21, 64, nv.NVFP4_SF_PREPACKED, 256, 256, 256, 256, 256)
     assert nv.lib.nvfp4_grouped_gemm_noalloc(1, (nv.Nvfp4Problem * 1)(big), None) == nv.NVFP4_ERR_TOO_LARGE
-    rowmajor = nv.Nvfp4Problem(128, 128, 256, nv.NVFP4_SF_ROWMAJOR, 256, 256, 256, 256, 256)
+    # row-major scales with K % 256 != 0 would need the prepack pass and its workspace
+    rowmajor = nv.Nvfp4Problem(128, 128, 320, nv.NVFP4_SF_ROWMAJOR, 256, 256, 256, 256, 256)
     assert nv.lib.nvfp4_grouped_gemm_noalloc(1, (nv.Nvfp4Problem * 1)(rowmajor), None) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_noalloc_reads_row_major_scales_where_k_is_a_multiple_of_256():
+    nv.lib.nvfp4_grouped_gemm_noalloc.restype = ctypes.c_int
+    nv.lib.nvfp4_grouped_gemm_noalloc.argtypes = [ctypes.c_int, ctypes.POINTER(nv.Nvfp4Problem), ctypes.c_void_p]
+    groups = gen.make_problem_set(33, [200, 64, 129, 3], [384, 256, 136, 8], [1536, 512, 768, 256])
+    # reference: the cached entry point on the same kernel (single CTAs, whole tiles)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 2)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 0)
+    try:
+        ref = [DeviceGroup(g) for g in groups]
+        nv.nvfp4_grouped_gemm([x.problem() for x in ref])
+        torch.cuda.synchronize()
+    finally:
+        nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 0)
+        nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 1)
+    d = [DeviceGroup(g, nv.NVFP4_SF_ROWMAJOR) for g in groups]
+    assert _noalloc(d) == nv.NVFP4_OK
+    torch.cuda.synchronize()
+    assert nv.nvfp4_last_launches() == 1
+    for g, x, r in zip(groups, d, ref):
+        got = x.result()
+        assert not np.isnan(got).any() and x.guards_intact()
+        # the same scales reach the MMAs by either route: the same bits
+        assert np.array_equal(got.view(np.uint16), r.result().view(np.uint16))
