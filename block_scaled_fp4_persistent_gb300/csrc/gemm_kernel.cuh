@@ -18,10 +18,10 @@
 //               16 bytes per stage (TMA tensor copies); the stagers transpose the
 //               latter on the way, so row-major scales need no separate pass.
 //   warps 6-13  epilogue. Two warps per TMEM lane quarter, each owning BN/2
-//               columns. They drain the accumulator 32 columns at a time, convert to
-//               fp16, and send each 32 x 32 block out through a swizzled shared-memory
-//               buffer and a TMA store (which clips rows past M and columns past N);
-//               the accumulator is freed for the next tile after the last TMEM read.
+//               columns. They read their columns of the accumulator (16 at a time)
+//               into fp16 registers and free it for the next tile, then send each
+//               32 x 32 block out through a swizzled shared-memory buffer and a TMA
+//               store (which clips rows past M and columns past N).
 //
 // Why this shape. Measurements on this GPU drove it:
 //  * One tcgen05.cp of a 512-byte scale block costs about as much tensor-pipe
@@ -31,8 +31,8 @@
 //    stage for its barrier wait and commit, whatever the MMA's N. N = 256 MMAs
 //    (BN = 256) halve the issue cost per output and the A re-reads per output.
 //  * With BN = 256 the accumulator takes half of TMEM. It is single-buffered:
-//    eight epilogue warps drain it in a few hundred cycles, and the next tile's
-//    MMAs start while those warps store the previous tile.
+//    eight epilogue warps read it out in ~0.45 us, and the next tile's MMAs start
+//    while those warps store the previous tile.
 //
 // The pages' kernels (page 1 `grouped_gemm_kernel_v4`, page 2
 // `group_gemm_kernel_impl`) copy the scales with tcgen05.cp from the MMA thread,

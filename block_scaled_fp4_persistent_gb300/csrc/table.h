@@ -100,10 +100,6 @@ struct Table {
     {
         return reinterpret_cast<const GroupEntry *>(reinterpret_cast<const char *>(this) + sizeof(TableHeader))[g];
     }
-    __host__ __device__ uint32_t cta_begin(int c) const
-    {
-        return reinterpret_cast<const uint32_t *>(reinterpret_cast<const char *>(this) + h.off_cta_begin)[c];
-    }
     int num_groups_host() const { return h.num_groups; }
 };
 
