@@ -43,6 +43,7 @@ NVFP4_OPT_PREFETCH_STAGES = 6
 NVFP4_OPT_SPLIT_TAIL = 7
 NVFP4_OPT_CTA_PAIR = 8
 NVFP4_OPT_SF_DIRECT = 9
+NVFP4_OPT_PDL = 10
 
 
 class Nvfp4Error(RuntimeError):

@@ -373,6 +373,9 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         // ring holds only STAGES stages, and a stage that comes from DRAM takes
         // ~1.5 us to land, while one that comes from L2 lands several times sooner.
         if (lane == 0) {
+            // Inputs may come from the previous kernel in the stream (programmatic
+            // dependent launch): nothing of the caller's is read before this wait.
+            grid_dependency_wait();
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
@@ -479,6 +482,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     }
                 }
             }
+            grid_launch_dependents();  // every copy of this CTA is issued
             // Before the CTA may exit, every copy it started must have landed.
             // A full barrier whose last fill was consumed has already flipped its
             // phase, so these waits return at once in a normal run.
@@ -605,6 +609,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
+        grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);

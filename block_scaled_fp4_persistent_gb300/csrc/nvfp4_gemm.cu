@@ -52,7 +52,32 @@ struct Options {
     std::atomic<int64_t> split_tail{1};  // 0 off, 1 single CTAs only, 2 single CTAs and pairs
     std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
     std::atomic<int64_t> sf_direct{1};  // 1 = row-major scales read by the GEMM kernel where K % 256 == 0
+    std::atomic<int64_t> pdl{0};  // 1 = GEMM launches with programmatic stream serialization
 } g_opt;
+
+// Launches one of the GEMM kernels. With the PDL option on, the launch allows
+// programmatic stream serialization: the kernel may start (set up barriers and
+// TMEM, read its own tables) while the previous kernel in the stream finishes;
+// it waits for that kernel before it reads or writes the caller's memory.
+template <class Kernel>
+cudaError_t launch_kernel(Kernel kernel, unsigned grid, size_t smem, cudaStream_t stream, const KernelArgs &args)
+{
+    if (g_opt.pdl.load() == 0) {
+        kernel<<<grid, kThreads, smem, stream>>>(args);
+        return cudaGetLastError();
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, args);
+}
 
 constexpr int kMaxDevices = 64;
 // Kernel variants: BLOCK_N 128 or 256, each with the deepest ring that fits in
@@ -632,8 +657,7 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.workspace = t.workspace;
     args.counters = t.counters;
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
-    nvfp4_grouped_gemm_kernel<BN, STAGES><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<BN, STAGES>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     static_assert(kDeepStages128 == 5 && kDeepStages256 == 3, "kernel names below");
     g_last_kernel.store(BN == 128 ? (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<128,2>" : "nvfp4_grouped_gemm_kernel<128,5>")
                                   : (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<256,2>" : "nvfp4_grouped_gemm_kernel<256,3>"));
@@ -678,8 +702,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.workspace = t.workspace;
     args.counters = t.counters;
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
-    nvfp4_pair_gemm_kernel<kPairStages><<<t.grid, kThreads, L::kSmemBytes, stream>>>(args);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launch_kernel(nvfp4_pair_gemm_kernel<kPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_pair_gemm_kernel<5>");
     return NVFP4_OK;
 }
@@ -921,6 +944,11 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         if (value < 0 || value > 2)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.split_tail = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_PDL:
+        if (value < 0 || value > 1)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.pdl = value;
         return NVFP4_OK;
     case NVFP4_OPT_SF_DIRECT:
         if (value < 0 || value > 1)
@@ -1204,8 +1232,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.workspace = nullptr;  // no split tiles here
     args.counters = nullptr;
     std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
-    nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages><<<grid, kThreads, Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream>>>(args);
-    CUDA_TRY(cudaGetLastError());
+    CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages>, (unsigned)grid,
+                           Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");
     g_last_launches.store(1);
     return NVFP4_OK;

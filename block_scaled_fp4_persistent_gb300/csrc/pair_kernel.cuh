@@ -148,6 +148,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     if (warp == kProducerWarp) {
         // ------------------------------------------------------ TMA producer
         if (lane == 0) {
+            // Inputs may come from the previous kernel in the stream (programmatic
+            // dependent launch): nothing of the caller's is read before this wait.
+            grid_dependency_wait();
             const uint64_t pol_a = policy_evict_last();
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
@@ -200,6 +203,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     }
                 }
             }
+            grid_launch_dependents();  // every copy of this CTA is issued
             // Every copy this CTA started must land before it may exit.
             const uint32_t issued = kiter < (uint32_t)STAGES ? kiter : (uint32_t)STAGES;
             for (uint32_t i = 0; i < issued; ++i) {
@@ -327,6 +331,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
+        grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);

@@ -39,6 +39,24 @@ __device__ __forceinline__ void named_barrier_arrive(uint32_t id, uint32_t threa
     asm volatile("bar.arrive %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// ---------------------------------------------- programmatic dependent launch --
+
+// Waits until the grids this one depends on (the previous kernel in the stream,
+// when this grid was launched with programmatic stream serialization) have
+// completed and their memory is visible. In any other launch it returns at once.
+__device__ __forceinline__ void grid_dependency_wait()
+{
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+}
+
+// Lets the next grid in the stream, if it was launched with programmatic stream
+// serialization, begin launching (it still waits for this grid before it touches
+// memory). Called once per CTA.
+__device__ __forceinline__ void grid_launch_dependents()
+{
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ----------------------------------------------------------------- cluster --
 
 // Rank of this CTA in its cluster (0 or 1 for a CTA pair).

@@ -181,6 +181,12 @@ int nvfp4_last_launches(void);
  *  NVFP4_OPT_SF_DIRECT     : 1 = row-major scales are read directly by the GEMM
  *                             kernel where K % 256 == 0 (default), 0 = always
  *                             prepacked by an extra launch first
+ *  NVFP4_OPT_PDL           : 0 = off (default), 1 = the GEMM kernel is launched
+ *                             with programmatic stream serialization: it may begin
+ *                             (barriers, TMEM, its tables) while the previous kernel
+ *                             in the stream finishes, and waits for that kernel
+ *                             (griddepcontrol.wait) before it reads or writes any of
+ *                             the caller's memory. For callers that chain kernels.
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
  *                             CTA 0 skips the copies of its k-stage with that
  *                             global index. The consumer's wait then runs out
@@ -196,7 +202,8 @@ enum {
     NVFP4_OPT_PREFETCH_STAGES = 6,
     NVFP4_OPT_SPLIT_TAIL = 7,
     NVFP4_OPT_CTA_PAIR = 8,
-    NVFP4_OPT_SF_DIRECT = 9
+    NVFP4_OPT_SF_DIRECT = 9,
+    NVFP4_OPT_PDL = 10
 };
 int nvfp4_set_option(int option, int64_t value);
 

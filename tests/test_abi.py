@@ -104,11 +104,13 @@ def test_options(nv):
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_WAIT_TIMEOUT_US, 0) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, 2) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, -1) == -1
+    assert lib.nvfp4_set_option(nv.NVFP4_OPT_PDL, 2) == -1
     for opt, val in [(nv.NVFP4_OPT_STAGES, 2), (nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_BLOCK_N, 256),
                      (nv.NVFP4_OPT_BLOCK_N, 128), (nv.NVFP4_OPT_MAX_CTAS, 3),
                      (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
                      (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_BLOCK_N, 0),
                      (nv.NVFP4_OPT_CTA_PAIR, 1), (nv.NVFP4_OPT_CTA_PAIR, 2), (nv.NVFP4_OPT_CTA_PAIR, 0),
                      (nv.NVFP4_OPT_SPLIT_TAIL, 2), (nv.NVFP4_OPT_SPLIT_TAIL, 0), (nv.NVFP4_OPT_SPLIT_TAIL, 1),
-                     (nv.NVFP4_OPT_SF_DIRECT, 0), (nv.NVFP4_OPT_SF_DIRECT, 1)]:
+                     (nv.NVFP4_OPT_SF_DIRECT, 0), (nv.NVFP4_OPT_SF_DIRECT, 1), (nv.NVFP4_OPT_PDL, 1),
+                     (nv.NVFP4_OPT_PDL, 0)]:
         assert lib.nvfp4_set_option(opt, val) == 0

@@ -27,7 +27,8 @@ def _defaults():
     yield
     for opt, val in [(nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_BLOCK_N, 0),
                      (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
-                     (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0), (nv.NVFP4_OPT_SF_DIRECT, 1)]:
+                     (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0), (nv.NVFP4_OPT_SF_DIRECT, 1),
+                     (nv.NVFP4_OPT_PDL, 0)]:
         nv.nvfp4_set_option(opt, val)
 
 
@@ -116,6 +117,44 @@ def test_row_major_scales_read_in_the_kernel(pair, block_n):
     for a, b, c in zip(d, pre, via):
         assert np.array_equal(a.result().view(np.uint16), b.result().view(np.uint16))
         assert np.array_equal(a.result().view(np.uint16), c.result().view(np.uint16))
+
+
+@pytest.mark.parametrize("pair", [1, 2])
+def test_dependent_launch_waits_for_the_kernels_before_it(pair):
+    # With programmatic dependent launch the GEMM may start while the kernel before
+    # it finishes. Here that kernel writes the right inputs over wrong ones, and a
+    # second GEMM call writes other results over the first call's C: the outputs
+    # must be those of the right inputs and of the second call.
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_PDL, 1)
+    first = gen.make_problem_set(81, [200, 64, 129], [384, 256, 136], [1536, 512, 768])
+    second = gen.make_problem_set(82, [200, 64, 129], [384, 256, 136], [1536, 512, 768])
+    d1 = [DeviceGroup(g) for g in first]
+    d2 = [DeviceGroup(g) for g in second]
+    right = [(x.A.clone(), x.B.clone()) for x in d1]
+    for x in d1:
+        x.A.fill_(0x77)
+        x.B.fill_(0x77)
+    zero = torch.zeros(1, dtype=torch.uint8, device="cuda")
+    torch.cuda.synchronize()
+    for x, (a, b) in zip(d1, right):
+        torch.bitwise_or(a, zero, out=x.A)  # kernels, right before the GEMM in the same stream
+        torch.bitwise_or(b, zero, out=x.B)
+    nv.nvfp4_grouped_gemm([x.problem() for x in d1])
+    torch.cuda.synchronize()
+    check_full(first, d1, f"dependent launch, inputs written just before, pair={pair}")
+    # two calls in a row into the same C: the second one's results must remain
+    probs2 = []
+    for x1, x2 in zip(d1, d2):
+        p = x2.problem()
+        p.C = x1.problem().C
+        probs2.append(p)
+    nv.nvfp4_grouped_gemm([x.problem() for x in d1])
+    nv.nvfp4_grouped_gemm(probs2)
+    torch.cuda.synchronize()
+    status, detail = nv.nvfp4_device_status()
+    assert status == 0, detail
+    check_full(second, d1, f"dependent launch, two calls into one C, pair={pair}")
 
 
 def test_structured_closed_form():
