@@ -120,6 +120,19 @@ def test_row_major_scales_read_in_the_kernel(pair, block_n):
 
 
 @pytest.mark.parametrize("pair", [1, 2])
+def test_dependent_launch_with_row_major_scales(pair):
+    # row-major scales with K % 256 != 0 for some groups: a prepack launch, then the
+    # dependent GEMM launch, which must wait for the prepacked scales
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_PDL, 1)
+    groups = gen.make_problem_set(RAGGED["seed"] + 2, RAGGED["Ms"], RAGGED["Ns"], RAGGED["Ks"])
+    d = [DeviceGroup(g, nv.NVFP4_SF_ROWMAJOR) for g in groups]
+    run(d)
+    assert nv.nvfp4_last_launches() == 2
+    check_full(groups, d, f"dependent launch after the prepack, pair={pair}")
+
+
+@pytest.mark.parametrize("pair", [1, 2])
 def test_dependent_launch_waits_for_the_kernels_before_it(pair):
     # With programmatic dependent launch the GEMM may start while the kernel before
     # it finishes. Here that kernel writes the right inputs over wrong ones, and a
