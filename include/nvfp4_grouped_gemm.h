@@ -89,13 +89,18 @@ typedef struct {
 } Nvfp4Problem;
 
 /* The grouped GEMM: one persistent kernel launch for all g problems (plus a
- * prepack launch when some scales are row-major, plus a memset per K == 0
- * group).
+ * prepack launch when some row-major scales have K % 256 != 0, plus a memset per
+ * K == 0 group).
  *
  * probs is read during the call only. The library keeps, per distinct problem
  * set, a device-side table: tensor maps, per-group pointers and the tile
  * schedule. The table is cached by a hash of probs, so a repeated call
  * uploads nothing.
+ *
+ * CUDA graphs: once a problem set has been called once outside a capture (its
+ * table, and any prepack workspace of the stream, then exist), a call records
+ * into a graph being captured on its stream: it allocates, uploads and
+ * synchronises nothing.
  *
  * g == 0 is a no-op and returns NVFP4_OK. Errors: see the enum above. A
  * timeout inside the kernel is reported only by nvfp4_device_status(). */

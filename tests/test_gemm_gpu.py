@@ -170,6 +170,30 @@ def test_dependent_launch_waits_for_the_kernels_before_it(pair):
     check_full(second, d1, f"dependent launch, two calls into one C, pair={pair}")
 
 
+@pytest.mark.parametrize("pair", [1, 2])
+def test_cuda_graph_capture_and_replay(pair):
+    # Once a problem set's table is cached, a call records into a CUDA graph (no
+    # allocation, no synchronisation inside) and the graph replays it.
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    groups = gen.make_problem_set(91, [200, 64, 129], [384, 256, 136], [1536, 512, 768])
+    d = [DeviceGroup(g) for g in groups]
+    probs = [x.problem() for x in d]
+    run(d)  # warms the table cache
+    for x in d:
+        x.reset()
+    torch.cuda.synchronize()
+    s = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        nv.nvfp4_grouped_gemm(probs, s.cuda_stream)
+    for _ in range(2):
+        for x in d:
+            x.reset()
+        graph.replay()
+        torch.cuda.synchronize()
+        check_full(groups, d, f"graph replay pair={pair}")
+
+
 def test_structured_closed_form():
     # all elements 1.0 with scales 0.5 and 2 (codes 0x30, 0x40): C = K exactly
     class G:
