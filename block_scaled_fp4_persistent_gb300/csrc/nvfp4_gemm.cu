@@ -711,13 +711,13 @@ int workspace_for(int dev, cudaStream_t stream, size_t bytes, void **out)
 {
     Workspace &w = g_workspaces[{dev, reinterpret_cast<uintptr_t>(stream)}];
     if (w.bytes < bytes) {
+        const size_t want = std::max(bytes, w.bytes * 2);  // grow geometrically
         if (w.ptr) {
             CUDA_TRY(cudaStreamSynchronize(stream));
             cudaFree(w.ptr);
             w.ptr = nullptr;
             w.bytes = 0;
         }
-        const size_t want = std::max(bytes, w.bytes * 2);
         CUDA_TRY(cudaMalloc(&w.ptr, want));
         w.bytes = want;
     }
