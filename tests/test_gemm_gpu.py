@@ -300,15 +300,15 @@ def sample_indices(M, N, n, rng):
     return np.array(ms), np.array(ns)
 
 
-@pytest.mark.parametrize("pair", [0, 1, 2])
+@pytest.mark.parametrize("pair,layout", [(0, nv.NVFP4_SF_PREPACKED), (1, nv.NVFP4_SF_ROWMAJOR),
+                                         (2, nv.NVFP4_SF_PREPACKED), (2, nv.NVFP4_SF_ROWMAJOR)])
 @pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
-def test_full_size_workloads_sampled(name, pair):
-    # pair 0: the automatic choice, the benchmark's launch configuration; 1: CTA pairs;
-    # 2: single CTAs. Pairs read row-major scales in the kernel (the e2e benchmark's
-    # route), the others prepacked ones.
+def test_full_size_workloads_sampled(name, pair, layout):
+    # pair 0: the automatic choice with prepacked scales, the benchmark's launch
+    # configuration; 1: CTA pairs; 2: single CTAs (which split the MoE sets' last
+    # wave along K). Row-major scales are read in the kernel (the e2e benchmark's route).
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_workload(name)
-    layout = nv.NVFP4_SF_ROWMAJOR if pair == 1 else nv.NVFP4_SF_PREPACKED
     d = [DeviceGroup(g, layout) for g in groups]
     run(d)  # default options: the launch configuration of the benchmark
     rng = np.random.default_rng(99)
