@@ -11,7 +11,7 @@ been built, the first call raises ImportError. Build it with
 Names match the C ABI: ``nvfp4_grouped_gemm``, ``nvfp4_prepack_scales``,
 ``nvfp4_prepacked_scale_bytes``, ``nvfp4_device_status``,
 ``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_last_kernel``, ``nvfp4_last_launches``,
-``nvfp4_set_option`` and
+``nvfp4_last_a_maps``, ``nvfp4_set_option`` and
 ``nvfp4_release``.
 """
 from __future__ import annotations
@@ -44,6 +44,7 @@ NVFP4_OPT_SPLIT_TAIL = 7
 NVFP4_OPT_CTA_PAIR = 8
 NVFP4_OPT_SF_DIRECT = 9
 NVFP4_OPT_PDL = 10
+NVFP4_OPT_M_FUSION = 11
 
 
 class Nvfp4Error(RuntimeError):
@@ -87,6 +88,8 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_last_kernel.argtypes = []
     lib.nvfp4_last_launches.restype = ctypes.c_int
     lib.nvfp4_last_launches.argtypes = []
+    lib.nvfp4_last_a_maps.restype = ctypes.c_int
+    lib.nvfp4_last_a_maps.argtypes = []
     lib.nvfp4_set_option.restype = ctypes.c_int
     lib.nvfp4_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.nvfp4_release.restype = None
@@ -168,6 +171,10 @@ def nvfp4_last_kernel() -> str:
 
 def nvfp4_last_launches() -> int:
     return _get().nvfp4_last_launches()
+
+
+def nvfp4_last_a_maps() -> int:
+    return _get().nvfp4_last_a_maps()
 
 
 def nvfp4_set_option(option: int, value: int) -> None:

@@ -394,7 +394,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 Src r;
                 const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: no load
-                r.tmap_a = &ge.tmap_a;
+                r.tmap_a = &ge.tmap_a;  // one A map per group: M-fusion is for CTA pairs only
                 r.tmap_b = &ge.tmap_b;
                 r.ya = w.tile_m * kBlockM;
                 r.yb = w.tile_n * BN;

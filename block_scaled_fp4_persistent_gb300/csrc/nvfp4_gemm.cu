@@ -41,6 +41,7 @@ namespace {
 std::atomic<int> g_last_cuda_error{0};
 std::atomic<const char *> g_last_kernel{"none"};  // the variant the last call launched
 std::atomic<int> g_last_launches{0};  // kernels the last GEMM call launched (prepack and GEMM)
+std::atomic<int> g_last_a_maps{0};    // A tensor maps the last GEMM call's table holds (M-fusion runs)
 
 struct Options {
     std::atomic<int64_t> block_n{0};
@@ -53,6 +54,7 @@ struct Options {
     std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
     std::atomic<int64_t> sf_direct{1};  // 1 = row-major scales read by the GEMM kernel where K % 256 == 0
     std::atomic<int64_t> pdl{0};  // 1 = GEMM launches with programmatic stream serialization
+    std::atomic<int64_t> m_fusion{1};  // 1 = groups whose A rows follow one another share one A map
 } g_opt;
 
 // Launches one of the GEMM kernels. With the PDL option on, the launch allows
@@ -121,6 +123,7 @@ struct CachedTable {
     int grid = 0;
     int block_n = 0;
     int variant = 0;  // the kernel variant the table was built for
+    int a_maps = 0;   // distinct A tensor maps: one per run of groups with consecutive A rows
     std::vector<uint32_t> list_begin;  // the table's cta_begin, passed again with each launch
 };
 // The device address of a cached table's work items.
@@ -317,13 +320,15 @@ WorkItem make_item(const ActiveGroup &g, int group, int m, int n, int kb_begin, 
     w.seg = seg;
     w.nseg = nseg;
     w.ws_slot = slot;
+    w.a_row = m * block_m;  // the group's own A map; M-fusion rebases it
     const int kb64 = g.K / 64;
     w.kblocks64 = kb64;
     const int row_tiles_a = (g.M + 127) / 128, row_tiles_b = (g.N + 127) / 128;
     const int ra = m * (block_m / 128), rb = n * (block_n / 128);
     w.flags = ((g.M + block_m - 1) / block_m > 1 ? kItemBShared : 0) |
               (block_m == 256 && ra + 1 < row_tiles_a ? kItemA2 : 0) |
-              (block_n == 256 && rb + 1 < row_tiles_b ? kItemB2 : 0) | (g.sf_rowmajor ? kItemSfRowMajor : 0);
+              (block_n == 256 && rb + 1 < row_tiles_b ? kItemB2 : 0) | (g.sf_rowmajor ? kItemSfRowMajor : 0) |
+              (group << kItemAMapShift);
     const size_t blocks = (size_t)kb64 * kScaleBlockBytes;
     w.sfa = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFA) + (size_t)ra * blocks);
     w.sfb = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFB) + (size_t)rb * blocks);
@@ -490,12 +495,60 @@ int choose_variant(const std::vector<ActiveGroup> &gs, const DeviceState &ds, in
     return t_pair < t_single ? kVariantPair : 0;
 }
 
+// M-fusion (page 2, `_merge_groups`). Active group i continues the run of group
+// i - 1 when its A rows follow that group's in memory (the caller passed slices of
+// one concatenated A) with the same K, and, where the kernel reads row-major scales,
+// its SFA rows follow too. A run shares its first group's A (and SFA) tensor map,
+// which spans the rows of the whole run; an item addresses its rows from the run's
+// first row. A tile's rows past its group's M are then the next group's rows rather
+// than TMA's zero fill: they reach only output rows that are never stored.
+struct ARuns {
+    std::vector<int> head;       // the run's first group
+    std::vector<int32_t> row0;   // the group's first row in the run's map
+    std::vector<int64_t> rows;   // at a run's first group: the rows of the run
+    int maps = 0;
+};
+
+bool rows_follow(const void *prev, size_t bytes, const void *next)
+{
+    return reinterpret_cast<uintptr_t>(prev) + bytes == reinterpret_cast<uintptr_t>(next);
+}
+
+ARuns a_runs(const std::vector<ActiveGroup> &gs, bool fuse)
+{
+    ARuns r;
+    const size_t n = gs.size();
+    r.head.resize(n);
+    r.row0.resize(n);
+    r.rows.assign(n, 0);
+    for (size_t i = 0; i < n; ++i) {
+        const ActiveGroup &q = gs[i];
+        bool join = fuse && i > 0;
+        if (join) {
+            const ActiveGroup &p = gs[i - 1];
+            join = p.K == q.K && p.sf_rowmajor == q.sf_rowmajor && rows_follow(p.A, (size_t)p.M * (p.K / 2), q.A) &&
+                   (!q.sf_rowmajor || rows_follow(p.SFA, (size_t)p.M * (p.K / 16), q.SFA)) &&
+                   r.rows[r.head[i - 1]] + q.M <= INT32_MAX;  // TMA row coordinates are 32-bit
+        }
+        if (join) {
+            r.head[i] = r.head[i - 1];
+            r.row0[i] = r.row0[i - 1] + gs[i - 1].M;
+        } else {
+            r.head[i] = (int)i;
+            r.row0[i] = 0;
+            ++r.maps;
+        }
+        r.rows[r.head[i]] += q.M;
+    }
+    return r;
+}
+
 // Caller holds g_mu. variant_req is a kernel variant or kVariantAuto.
 int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs, int variant_req, int64_t max_ctas,
-              int split_mode, cudaStream_t stream, CachedTable **out)
+              int split_mode, int m_fusion, cudaStream_t stream, CachedTable **out)
 {
     std::vector<uint8_t> sig(sizeof(int) * 5 + gs.size() * sizeof(ActiveGroup));
-    int hdr[5] = {dev, variant_req, (int)std::min<int64_t>(max_ctas, 1 << 30), 0, split_mode};
+    int hdr[5] = {dev, variant_req, (int)std::min<int64_t>(max_ctas, 1 << 30), m_fusion, split_mode};
     memcpy(sig.data(), hdr, sizeof(hdr));
     if (!gs.empty())
         memcpy(sig.data() + sizeof(hdr), gs.data(), gs.size() * sizeof(ActiveGroup));
@@ -516,6 +569,14 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     const int block_m = plan.block_m, block_n = plan.block_n;
     const int halves = pair ? 2 : 1;  // workspace slots and counters per split segment / tile
     Schedule sc = build_schedule(gs, block_m, block_n, plan.grid_cap, split_for(variant, split_mode));
+    // M-fusion for the pair kernel only: the single-CTA kernel addressing A through
+    // the item's row rather than its tile index measured ~1 us slower on the small
+    // two-group sets it serves (which have no runs to fuse anyway).
+    const ARuns runs = a_runs(gs, m_fusion != 0 && pair);
+    for (WorkItem &w : sc.items) {
+        w.a_row += runs.row0[w.group];
+        w.flags = (w.flags & ((1 << kItemAMapShift) - 1)) | (runs.head[w.group] << kItemAMapShift);
+    }
     const std::vector<WorkItem> &items = sc.items;
     const std::vector<uint32_t> &cta_begin = sc.list_begin;
     const int grid = sc.grid;  // lists: CTAs, or CTA pairs
@@ -533,6 +594,7 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     t.grid = grid * halves;
     t.block_n = block_n;
     t.variant = variant;
+    t.a_maps = runs.maps;
     t.list_begin = sc.list_begin;
     CUDA_TRY(cudaMallocHost(&t.host, total));
     memset(t.host, 0, total);
@@ -549,14 +611,27 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     for (size_t i = 0; i < gs.size(); ++i) {
         const ActiveGroup &a = gs[i];
         GroupEntry &e = ge[i];
-        int rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, (uint64_t)a.M, kBlockM);
+        const int h = runs.head[i];
+        const uint64_t run_rows = (uint64_t)runs.rows[h];
+        // A run's later groups keep a copy of its map, so every group's maps stay
+        // valid descriptors; the items read the first group's.
+        int rc = 0;
+        if (h == (int)i)
+            rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, run_rows, kBlockM);
+        else
+            e.tmap_a = ge[h].tmap_a;
         if (!rc)
             rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, pair ? 128u : (uint32_t)block_n);
         if (!rc)
             rc = encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
-        if (!rc)
-            rc = a.sf_rowmajor ? encode_scale_map(&e.tmap_sfa, a.SFA, (uint64_t)a.K / 16, (uint64_t)a.M, kBlockM)
-                               : encode_unused_scale_map(&e.tmap_sfa, a.SFA);
+        if (!rc) {
+            if (!a.sf_rowmajor)
+                rc = encode_unused_scale_map(&e.tmap_sfa, a.SFA);
+            else if (h == (int)i)
+                rc = encode_scale_map(&e.tmap_sfa, a.SFA, (uint64_t)a.K / 16, run_rows, kBlockM);
+            else
+                e.tmap_sfa = ge[h].tmap_sfa;
+        }
         if (!rc)
             rc = a.sf_rowmajor ? encode_scale_map(&e.tmap_sfb, a.SFB, (uint64_t)a.K / 16, (uint64_t)a.N,
                                                   pair ? (uint32_t)kPairBlockN : (uint32_t)block_n)
@@ -738,6 +813,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         return NVFP4_OK;
     if (!probs)
         return NVFP4_ERR_INVALID_ARG;
+    if (g >= kMaxGroups)
+        return NVFP4_ERR_TOO_LARGE;
     for (int i = 0; i < g; ++i)
         if (int rc = check_problem(probs[i]))
             return rc;
@@ -813,7 +890,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
         if (int rc = prepare_pair_kernel(*ds))  // also learns how many CTA pairs fit at once
             return rc;
     CachedTable *t = nullptr;
-    if (int rc2 = get_table(dev, *ds, gs, variant_req, g_opt.max_ctas.load(), (int)g_opt.split_tail.load(), stream, &t))
+    if (int rc2 = get_table(dev, *ds, gs, variant_req, g_opt.max_ctas.load(), (int)g_opt.split_tail.load(),
+                            (int)g_opt.m_fusion.load(), stream, &t))
         return rc2;
     const int variant = t->variant;
     int rc = NVFP4_OK;
@@ -833,8 +911,10 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     case 3: rc = launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size()); break;
     default: rc = launch_pair(*ds, *t, stream, (int)gs.size()); break;
     }
-    if (rc == NVFP4_OK)
+    if (rc == NVFP4_OK) {
         g_last_launches.store(prepack_launches + 1);
+        g_last_a_maps.store(t->a_maps);
+    }
     return rc;
 }
 
@@ -917,6 +997,8 @@ extern "C" const char *nvfp4_last_kernel(void) { return g_last_kernel.load(); }
 
 extern "C" int nvfp4_last_launches(void) { return g_last_launches.load(); }
 
+extern "C" int nvfp4_last_a_maps(void) { return g_last_a_maps.load(); }
+
 extern "C" int nvfp4_set_option(int option, int64_t value)
 {
     switch (option) {
@@ -949,6 +1031,11 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         if (value < 0 || value > 1)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.pdl = value;
+        return NVFP4_OK;
+    case NVFP4_OPT_M_FUSION:
+        if (value < 0 || value > 1)
+            return NVFP4_ERR_INVALID_ARG;
+        g_opt.m_fusion = value;
         return NVFP4_OK;
     case NVFP4_OPT_SF_DIRECT:
         if (value < 0 || value > 1)
@@ -1100,6 +1187,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
         return NVFP4_OK;
     if (!probs)
         return NVFP4_ERR_INVALID_ARG;
+    if (g >= kMaxGroups)
+        return NVFP4_ERR_TOO_LARGE;
     for (int i = 0; i < g; ++i) {
         if (int rc = check_problem(probs[i]))
             return rc;
@@ -1236,5 +1325,6 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
                            Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");
     g_last_launches.store(1);
+    g_last_a_maps.store(ngroups);  // no M-fusion here: one A map per group
     return NVFP4_OK;
 }

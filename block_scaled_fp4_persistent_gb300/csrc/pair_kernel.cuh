@@ -159,8 +159,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: the tensor maps
+                const GroupEntry &ga = tab->group(w.flags >> kItemAMapShift);  // the (possibly shared) A map
                 const int kb64 = w.kblocks64;
-                const int32_t ya = w.tile_m * kPairBlockM + (int)rank * 128;
+                const int32_t ya = w.a_row + (int)rank * 128;
                 const int32_t yb = w.tile_n * kPairBlockN + (int)rank * 128;
                 // Scale blocks come in 128-row tiles. A 128-row half that lies wholly
                 // past M (or N) reads the tile's first half's scales instead: its
@@ -183,10 +184,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_addr(&full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!(args.fault_skip_load >= 0 && blockIdx.x == 0 && kiter == (uint32_t)args.fault_skip_load)) {
-                        tma_load_2d(slot, &ge.tmap_a, kb * kRowBytes, ya, fb, pol_a);
+                        tma_load_2d(slot, &ga.tmap_a, kb * kRowBytes, ya, fb, pol_a);
                         tma_load_2d(slot + L::kOffB, &ge.tmap_b, kb * kRowBytes, yb, fb, pol_b);
                         if (sf_rm) {  // K % 256 == 0: a whole stage; B's box is both halves, 256 rows
-                            tma_load_2d(slot + L::kOffSfa, &ge.tmap_sfa, kb * kSfRowBytes, ya, fb, pol_a);
+                            tma_load_2d(slot + L::kOffSfa, &ga.tmap_sfa, kb * kSfRowBytes, ya, fb, pol_a);
                             tma_load_2d(slot + L::kOffSfb, &ge.tmap_sfb, kb * kSfRowBytes, w.tile_n * kPairBlockN, fb,
                                         pol_b);
                         } else {

@@ -59,8 +59,12 @@ struct WorkItem {
     int32_t nseg;
     int32_t ws_slot;
     int32_t kblocks64;
-    int32_t flags;  // kItemBShared | kItemA2 | kItemB2 | kItemSfRowMajor
-    int32_t reserved;
+    int32_t flags;  // kItemBShared | kItemA2 | kItemB2 | kItemSfRowMajor | a_map << kItemAMapShift
+    // Row of the tile's first A row in the A tensor map of group a_map (and, for
+    // row-major scales, in its SFA map). Groups whose A rows follow one another in
+    // memory share one map (M-fusion): the map of the first group of the run. Read
+    // by the pair kernel; the single-CTA kernel's tables are never fused.
+    int32_t a_row;
     const uint8_t *sfa;  // scale blocks of the tile's first 128 A rows (kblocks64 blocks of 512 B)
     const uint8_t *sfb;  // scale blocks of the tile's first 128 B rows
 };
@@ -69,6 +73,8 @@ constexpr int32_t kItemBShared = 1;  // the group has several m-tiles: its B til
 constexpr int32_t kItemA2 = 2;       // rows 128..255 of the tile's A rows exist (their scales follow sfa)
 constexpr int32_t kItemB2 = 4;       // rows 128..255 of the tile's B rows exist (their scales follow sfb)
 constexpr int32_t kItemSfRowMajor = 8;  // the group's scales are row-major, read through tmap_sfa / tmap_sfb
+constexpr int kItemAMapShift = 8;       // flags >> kItemAMapShift: the group whose tmap_a (tmap_sfa) the item reads
+constexpr int kMaxGroups = 1 << 23;     // a_map fits the flags' upper bits
 
 static_assert(sizeof(WorkItem) == 64, "WorkItem is read as four int4");
 
@@ -78,7 +84,7 @@ __host__ __device__ inline WorkItem unpack_item(int4 a, int4 b, int4 c, int4 d)
     WorkItem w;
     w.group = a.x, w.tile_m = a.y, w.tile_n = a.z, w.kb_begin = a.w;
     w.kb_end = b.x, w.split = b.y, w.seg = b.z, w.nseg = b.w;
-    w.ws_slot = c.x, w.kblocks64 = c.y, w.flags = c.z, w.reserved = c.w;
+    w.ws_slot = c.x, w.kblocks64 = c.y, w.flags = c.z, w.a_row = c.w;
     w.sfa = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.x | ((uint64_t)(uint32_t)d.y << 32));
     w.sfb = reinterpret_cast<const uint8_t *>((uint64_t)(uint32_t)d.z | ((uint64_t)(uint32_t)d.w << 32));
     return w;

@@ -47,7 +47,7 @@ enum {
     NVFP4_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 (sm_103a) */
     NVFP4_ERR_CUDA = -4,               /* a CUDA runtime or driver call failed; see nvfp4_last_cuda_error() */
     NVFP4_ERR_TIMEOUT = -5,            /* a kernel gave up a bounded wait; reported by nvfp4_device_status() */
-    NVFP4_ERR_TOO_LARGE = -6           /* a size beyond the library's limits (e.g. M, N or K >= 2^24) */
+    NVFP4_ERR_TOO_LARGE = -6           /* a size beyond the library's limits (e.g. M, N or K >= 2^24, or 2^23 groups) */
 };
 
 /* Scale-factor layouts of SFA/SFB. */
@@ -151,6 +151,11 @@ const char *nvfp4_last_kernel(void);
  * 0 before the first launch. */
 int nvfp4_last_launches(void);
 
+/* How many A tensor maps the table of the last successful GEMM call holds: the
+ * number of active groups, less one for every group that continues an M-fusion
+ * run (NVFP4_OPT_M_FUSION); 0 before the first launch. */
+int nvfp4_last_a_maps(void);
+
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
  *  NVFP4_OPT_CTA_PAIR      : 0 = automatic, 1 = CTA pairs, 2 = single CTAs.
@@ -192,6 +197,19 @@ int nvfp4_last_launches(void);
  *                             in the stream finishes, and waits for that kernel
  *                             (griddepcontrol.wait) before it reads or writes any of
  *                             the caller's memory. For callers that chain kernels.
+ *  NVFP4_OPT_M_FUSION      : 1 = on (default), 0 = off. M-fusion (page 2 of the
+ *                             sources, `_merge_groups`), on CTA pairs (the kernel for
+ *                             the many-group sets): consecutive active groups
+ *                             with the same K whose A rows follow one another in
+ *                             memory (A of group i+1 starts where group i's M rows
+ *                             end, as when the caller passes slices of one
+ *                             concatenated A) share one A tensor map spanning the
+ *                             run, and for row-major scales read by the kernel, one
+ *                             SFA map (their SFA rows must follow one another too).
+ *                             Results are the same bits either way; N may differ
+ *                             within a run. A tile's rows past its group's M then
+ *                             read the next group's rows, which only reach output
+ *                             rows that are never written.
  *  NVFP4_OPT_FAULT_SKIP_LOAD: -1 = off (default). Otherwise the producer of
  *                             CTA 0 skips the copies of its k-stage with that
  *                             global index. The consumer's wait then runs out
@@ -208,7 +226,8 @@ enum {
     NVFP4_OPT_SPLIT_TAIL = 7,
     NVFP4_OPT_CTA_PAIR = 8,
     NVFP4_OPT_SF_DIRECT = 9,
-    NVFP4_OPT_PDL = 10
+    NVFP4_OPT_PDL = 10,
+    NVFP4_OPT_M_FUSION = 11
 };
 int nvfp4_set_option(int option, int64_t value);
 

@@ -89,6 +89,7 @@ def test_trivial_calls_do_not_touch_cuda(nv):
     assert nv.lib.nvfp4_prepack_scales(8, 4, 64, 256, None) == -2
     assert nv.nvfp4_last_kernel() == "none"  # nothing launched in a process without a GPU
     assert nv.nvfp4_last_launches() == 0
+    assert nv.nvfp4_last_a_maps() == 0
 
 
 def test_options(nv):
@@ -105,6 +106,8 @@ def test_options(nv):
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, 2) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, -1) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_PDL, 2) == -1
+    assert lib.nvfp4_set_option(nv.NVFP4_OPT_M_FUSION, 2) == -1
+    assert lib.nvfp4_set_option(nv.NVFP4_OPT_M_FUSION, -1) == -1
     for opt, val in [(nv.NVFP4_OPT_STAGES, 2), (nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_BLOCK_N, 256),
                      (nv.NVFP4_OPT_BLOCK_N, 128), (nv.NVFP4_OPT_MAX_CTAS, 3),
                      (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
@@ -112,5 +115,5 @@ def test_options(nv):
                      (nv.NVFP4_OPT_CTA_PAIR, 1), (nv.NVFP4_OPT_CTA_PAIR, 2), (nv.NVFP4_OPT_CTA_PAIR, 0),
                      (nv.NVFP4_OPT_SPLIT_TAIL, 2), (nv.NVFP4_OPT_SPLIT_TAIL, 0), (nv.NVFP4_OPT_SPLIT_TAIL, 1),
                      (nv.NVFP4_OPT_SF_DIRECT, 0), (nv.NVFP4_OPT_SF_DIRECT, 1), (nv.NVFP4_OPT_PDL, 1),
-                     (nv.NVFP4_OPT_PDL, 0)]:
+                     (nv.NVFP4_OPT_PDL, 0), (nv.NVFP4_OPT_M_FUSION, 0), (nv.NVFP4_OPT_M_FUSION, 1)]:
         assert lib.nvfp4_set_option(opt, val) == 0

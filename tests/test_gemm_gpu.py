@@ -28,7 +28,7 @@ def _defaults():
     for opt, val in [(nv.NVFP4_OPT_STAGES, 0), (nv.NVFP4_OPT_MAX_CTAS, 0), (nv.NVFP4_OPT_BLOCK_N, 0),
                      (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_WAIT_TIMEOUT_US, 2000000),
                      (nv.NVFP4_OPT_SPLIT_TAIL, 1), (nv.NVFP4_OPT_CTA_PAIR, 0), (nv.NVFP4_OPT_SF_DIRECT, 1),
-                     (nv.NVFP4_OPT_PDL, 0)]:
+                     (nv.NVFP4_OPT_PDL, 0), (nv.NVFP4_OPT_M_FUSION, 1)]:
         nv.nvfp4_set_option(opt, val)
 
 
