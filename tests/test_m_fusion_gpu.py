@@ -84,10 +84,12 @@ def _fused(view, a_maps):
     return view.results()
 
 
+@pytest.mark.parametrize("split", [1, 2], ids=["split-single", "split-all"])
 @pytest.mark.parametrize("pair", [1, 2], ids=["pairs", "single"])
 @pytest.mark.parametrize("layout", [nv.NVFP4_SF_PREPACKED, nv.NVFP4_SF_ROWMAJOR], ids=["prepacked", "rowmajor"])
-def test_concatenated_a_is_one_map_and_the_same_bits(pair, layout):
+def test_concatenated_a_is_one_map_and_the_same_bits(pair, layout, split):
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, split)  # 2: split tails on pairs too, items cut along K
     # one K (1536: whole 256-wide stages, so row-major scales are read directly), ragged M, mixed N
     groups = gen.make_problem_set(41, [200, 64, 129, 3, 256, 77], [384, 256, 136, 8, 512, 264], [1536] * 6)
     dgroups = [DeviceGroup(g, layout) for g in groups]
