@@ -298,13 +298,6 @@ __device__ __forceinline__ void tc_fence_after()
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// Copies a 32-row x 16-byte block of shared memory (described by `desc`) into
-// TMEM columns taddr .. taddr+3, repeated in all four 32-lane quarters.
-__device__ __forceinline__ void tc_copy_scales(uint32_t taddr, uint64_t desc)
-{
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(desc) : "memory");
-}
-
 // D[tmem] (+)= A[smem] . B[smem]^T with E2M1 operands and one UE4M3 scale per
 // 16 K (scale vectors in TMEM); M = 128, N from idesc, K = 64.
 __device__ __forceinline__ void tc_mma_nvfp4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
