@@ -5,7 +5,8 @@
 //    slots; a whole tile has split = -1;
 //  * with split_tail on and uniform K, the CTAs' stage counts differ by at most one
 //    plus one tile's worth less than the whole-tile share, i.e. max - min <= nk;
-//  * the list offsets are monotone and end at the item count.
+//  * the list offsets are monotone and end at the item count;
+//  * M-fusion runs form where A rows follow one another, and only there.
 #include "nvfp4_gemm.cu"
 #include "prepack.cu"
 
@@ -158,6 +159,46 @@ int main()
         CHECK(choose_variant(g2a, ds, 0, 1) == 0, "g2 K=1536 -> single");
         CHECK(choose_variant(g2b, ds, 0, 1) == 0, "g2 K=4096 -> single");
         CHECK(choose_variant(tiny, ds, 0, 1) == 0, "tiny -> single");
+    }
+    // M-fusion runs (a_runs): A rows that follow one another with the same K join the
+    // previous group's run; a gap, a change of K or of the scale layout, row-major SFA rows
+    // that do not follow, or a run longer than 32-bit row coordinates starts a new one.
+    {
+        auto P = [](uintptr_t x) { return reinterpret_cast<const void *>(x); };
+        auto AG = [&](int M, int K, uintptr_t a, int rm = 0, uintptr_t sfa = 0x100000) {
+            return ActiveGroup{M, 256, K, rm, P(a), P(0x1000), P(sfa), P(0x2000), nullptr};
+        };
+        const uintptr_t base = 0x10000000;
+        // 3 contiguous groups (K = 1024: 512 bytes per row), then a gap, then 2 contiguous
+        std::vector<ActiveGroup> gs = {AG(100, 1024, base), AG(37, 1024, base + 100 * 512),
+                                       AG(5, 1024, base + 137 * 512), AG(64, 1024, base + 142 * 512 + 4096),
+                                       AG(1, 1024, base + 206 * 512 + 4096)};
+        ARuns r = a_runs(gs, true);
+        CHECK(r.maps == 2, "runs: %d maps", r.maps);
+        CHECK(r.head[0] == 0 && r.head[1] == 0 && r.head[2] == 0 && r.head[3] == 3 && r.head[4] == 3, "run heads");
+        CHECK(r.row0[1] == 100 && r.row0[2] == 137 && r.row0[4] == 64, "run rows");
+        CHECK(r.rows[0] == 142 && r.rows[3] == 65, "run lengths");
+        r = a_runs(gs, false);
+        CHECK(r.maps == 5 && r.head[2] == 2 && r.row0[2] == 0 && r.rows[2] == 5, "fusion off");
+        // a change of K breaks a run even where the bytes follow
+        gs = {AG(100, 1024, base), AG(50, 512, base + 100 * 512)};
+        CHECK(a_runs(gs, true).maps == 2, "K change");
+        // row-major scales: SFA rows (K/16 bytes each) must follow too; a layout change breaks
+        gs = {AG(100, 1024, base, 1, 0x200000), AG(50, 1024, base + 100 * 512, 1, 0x200000 + 100 * 64)};
+        CHECK(a_runs(gs, true).maps == 1, "row-major SFA follows");
+        gs[1].SFA = P(0x200000 + 100 * 64 + 16);
+        CHECK(a_runs(gs, true).maps == 2, "row-major SFA gap");
+        gs = {AG(100, 1024, base, 0), AG(50, 1024, base + 100 * 512, 1)};
+        CHECK(a_runs(gs, true).maps == 2, "layout change");
+        // 32-bit row coordinates: a run stops before passing INT32_MAX rows
+        gs.clear();
+        uintptr_t a = base;
+        for (int i = 0; i < 200; ++i) {
+            gs.push_back(AG(1 << 24, 64, a));
+            a += (size_t)(1 << 24) * 32;
+        }
+        r = a_runs(gs, true);
+        CHECK(r.maps == 2 && r.rows[0] == 127LL * (1 << 24) && r.head[127] == 127, "row limit: %d maps", r.maps);
     }
     std::printf(fails ? "FAILED %d\n" : "ok\n", fails);
     return fails ? 1 : 0;
