@@ -124,3 +124,20 @@ def test_runs_break_where_rows_or_k_do_not_follow():
     got = _fused(FusedView(dgroups, [[0, 1, 2, 3, 4]]), 2)
     for i, (r, c) in enumerate(zip(ref, got)):
         assert np.array_equal(c.view(np.uint16), r.view(np.uint16)), f"group {i}, across K"
+
+
+@pytest.mark.parametrize("layout", [nv.NVFP4_SF_PREPACKED, nv.NVFP4_SF_ROWMAJOR], ids=["prepacked", "rowmajor"])
+@pytest.mark.parametrize("name", ["moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
+def test_full_size_moe_with_concatenated_a(name, layout):
+    # the MoE layout: every expert's tokens are consecutive rows of one activation tensor
+    groups = gen.make_workload(name)
+    dgroups = [DeviceGroup(g, layout) for g in groups]
+    ref = _reference(dgroups)  # separate buffers, one map per group, automatic kernel choice (pairs)
+    got = _fused(FusedView(dgroups, [list(range(len(groups)))]), 1)
+    rng = np.random.default_rng(7)
+    for i, (g, r, c) in enumerate(zip(groups, ref, got)):
+        assert np.array_equal(c.view(np.uint16), r.view(np.uint16)), f"{name} group {i}"
+        ms = np.concatenate([rng.integers(0, g.M, 500), [0, g.M - 1]])
+        ns = np.concatenate([rng.integers(0, g.N, 500), [g.N - 1, 0]])
+        c_ref, s_ref = oracle.gemm_entries(g, ms, ns)
+        assert_within_bound(c[ms, ns], c_ref, s_ref, f"{name} group {i}, fused")
