@@ -1,4 +1,5 @@
-"""bench.py's multi-rank logic on CPU: two gloo ranks agree on the max time and pass the barrier.
+"""bench.py on CPU: two gloo ranks agree on the max time and pass the barrier; the reference arm
+(the oracle timed on the host cores) prints one line of the contract; warm-up below 3 is refused.
 (On GPUs the same functions run over NCCL. There, every rank runs its own replica and there
 is no collective on the data path.)"""
 import os
@@ -40,3 +41,30 @@ def test_single_rank_is_identity():
     import bench
     assert bench.reduce_max(3.25, 1) == 3.25
     bench.barrier(1)
+
+
+def test_reference_arm_prints_one_contract_line():
+    # the reference arm times the oracle on the host cores: no GPU needed
+    import json
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--workload", "tiny_g2",
+                        "--steps", "3", "--warmup", "3"], capture_output=True, text=True, timeout=600, cwd=root)
+    assert r.returncode == 0, r.stderr
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["impl"] == "reference" and d["unit"] == "us" and d["higher_is_better"] is False
+    assert d["value"] > 0 and d["steps"] == 3 and d["warmup"] == 3 and d["config"]["workload"] == "tiny_g2"
+    assert d["cpu_baseline"]["kind"] == "oracle" and d["cpu_baseline"]["cores"] >= 1
+    assert d["e2e"]["h2d_bytes_per_step"] == 0 and d["e2e"]["value"] == d["value"]
+
+
+def test_warmup_below_three_is_refused():
+    import subprocess
+    import sys
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    r = subprocess.run([sys.executable, os.path.join(root, "bench.py"), "--impl", "reference", "--warmup", "1"],
+                       capture_output=True, text=True, timeout=120, cwd=root)
+    assert r.returncode != 0 and "--warmup must be >= 3" in r.stderr
