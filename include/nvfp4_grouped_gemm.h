@@ -94,8 +94,11 @@ typedef struct {
  *
  * probs is read during the call only. The library keeps, per distinct problem
  * set, a device-side table: tensor maps, per-group pointers and the tile
- * schedule. The table is cached by a hash of probs, so a repeated call
- * uploads nothing.
+ * schedule (and, where the schedule splits tiles along K, their fp32 workspace
+ * and counters). The table is cached by a hash of probs, so a repeated call
+ * uploads nothing. Calls on different streams may overlap on the GPU when their
+ * problem sets differ; calls with the same problem set write the same C and
+ * share its table, so they must not overlap.
  *
  * CUDA graphs: once a problem set has been called once outside a capture (its
  * table, and any prepack workspace of the stream, then exist), a call records

@@ -292,6 +292,28 @@ def test_streams_are_respected():
     check_full(groups, d, "side stream")
 
 
+def test_two_streams_at_once_with_split_tails():
+    # Different problem sets on two streams, queued back to back without a sync: each has its own
+    # table, split workspace and counters. Single CTAs on a grid small enough to split the tails.
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 2)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, 70)
+    sets = [gen.make_problem_set(23, [130, 60, 200, 129], [2048, 1024, 1536, 520], [2048] * 4),
+            gen.make_problem_set(24, [100, 33, 250], [1536, 2048, 1024], [1024] * 3)]
+    dev = [[DeviceGroup(g) for g in groups] for groups in sets]
+    streams = [torch.cuda.Stream(), torch.cuda.Stream()]
+    torch.cuda.synchronize()
+    for _ in range(3):  # the first call of each set builds its table; later ones overlap
+        for d, st in zip(dev, streams):
+            with torch.cuda.stream(st):
+                nv.nvfp4_grouped_gemm([x.problem() for x in d], st)
+    torch.cuda.synchronize()
+    for st in streams:
+        status, detail = nv.nvfp4_device_status(st)
+        assert status == 0, f"device status {status}: {detail}"
+    for groups, d in zip(sets, dev):
+        check_full(groups, d, "two streams")
+
+
 # --------------------------------------------------------- full-size, sampled ---
 
 def sample_indices(M, N, n, rng):
