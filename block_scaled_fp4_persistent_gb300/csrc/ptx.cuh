@@ -438,10 +438,6 @@ __host__ __device__ constexpr uint64_t smem_desc(uint32_t addr, uint32_t lbo, ui
 // 8-row groups (1024 bytes) follow each other, so the stride offset is 1024.
 __host__ __device__ constexpr uint64_t operand_desc(uint32_t addr) { return smem_desc(addr, 16, 1024, 2); }
 
-// 32 rows x 16 bytes of scale bytes, unswizzled: 8-row core blocks of 128 bytes
-// follow each other, so the stride offset is 128.
-__host__ __device__ constexpr uint64_t scale_desc(uint32_t addr) { return smem_desc(addr, 16, 128, 0); }
-
 // Instruction descriptor of kind::mxf4nvf4 (E2M1 x E2M1, UE4M3 scales, fp32 D):
 //   bits  7-9  A format: 1 = E2M1          bits 10-11 B format: 1 = E2M1
 //   bits 15/16 A/B transpose: 0 = K-major  bits 17-22 N >> 3
