@@ -25,6 +25,9 @@ Timing (ours):
    row-major scales. Each timed step copies A, B, SFA and SFB host->device,
    runs the GEMM (which reads row-major scales itself where K % 256 == 0, else
    after a prepack launch), and copies C device->host.
+ * With the default workload on one GPU, the line also carries `other_workloads`:
+   the second MoE-shaped problem (N = 7168, K = 2048) timed the same way, not
+   part of `value` (--no-other-workloads skips it).
  * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
    scaling; the path has no exchange step). Timing is the max over ranks, and
    `value` = that time divided by N (aggregate time per grouped call).
@@ -470,6 +473,50 @@ def run_ours(args, groups, rank, world, local_rank):
     return out
 
 
+def time_flushed(groups, steps, warmup, local_rank):
+    """The headline protocol (L2 flushed before every call, CUDA events around each call)
+    on another workload, for the line's other_workloads key: mean us per call and the kernel."""
+    import torch
+    import block_scaled_fp4_persistent_gb300 as nv
+
+    dev = torch.device("cuda", local_rank)
+    stream = torch.cuda.current_stream()
+    keep, probs = [], []
+    for g in groups:
+        A = torch.from_numpy(g.A).to(dev)
+        B = torch.from_numpy(g.B).to(dev)
+        SFA = nv.prepack_scales(torch.from_numpy(g.SFA).to(dev), g.K)
+        SFB = nv.prepack_scales(torch.from_numpy(g.SFB).to(dev), g.K)
+        C = torch.empty((g.M, g.N), dtype=torch.float16, device=dev)
+        keep.append((A, B, SFA, SFB, C))
+        probs.append(nv.problem(A, B, SFA, SFB, C))
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush_w = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush_r = torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+    sink = torch.zeros(1, dtype=torch.float32, device=dev)
+
+    def flush():
+        flush_w.fill_(1.0)
+        torch.sum(flush_r, dim=(0,), keepdim=True, out=sink)
+
+    for _ in range(warmup):
+        flush()
+        nv.nvfp4_grouped_gemm(probs, stream)
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush()
+        starts[i].record(stream)
+        nv.nvfp4_grouped_gemm(probs, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    st, detail = nv.nvfp4_device_status(stream)
+    if st != 0:
+        raise RuntimeError(f"device status {st} {detail}")
+    return statistics.fmean(s.elapsed_time(e) for s, e in zip(starts, ends)) * 1e3, nv.nvfp4_last_kernel()
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -480,6 +527,8 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle timing sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-other-workloads", action="store_true",
+                    help="skip timing the second MoE workload beside the default one")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -532,6 +581,17 @@ def main():
     # each rank draws its own replica of the workload (weak scaling)
     groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
     out = run_ours(args, groups, rank, world, local_rank)
+    if world == 1 and args.workload == "moe_g8_n4096_k7168" and not args.no_other_workloads:
+        # the other MoE-shaped workload, timed the same way (not part of the headline value)
+        other = "moe_g8_n7168_k2048"
+        other_groups = gen.make_workload(other)
+        us, kern = time_flushed(other_groups, min(args.steps, 2000), args.warmup, local_rank)
+        peaks, _ = load_peaks()
+        _, _, _, t_fp4, t_hbm = roofline_terms(other_groups, peaks)
+        out["other_workloads"] = {other: {"value": round(us, 3), "unit": "us", "steps": min(args.steps, 2000),
+                                          "roofline_fraction": round(max(t_fp4, t_hbm) / us, 4), "kernel": kern,
+                                          "vs_baseline": round(us / PAGES_BEST_US[other], 4),
+                                          "l2": "flushed before every timed call"}}
     if rank == 0:
         if not args.no_cpu_baseline:
             threads = os.cpu_count() or 1
