@@ -26,8 +26,14 @@ Timing (ours):
    runs the GEMM (which reads row-major scales itself where K % 256 == 0, else
    after a prepack launch), and copies C device->host.
  * With the default workload on one GPU, the line also carries `other_workloads`:
-   the second MoE-shaped problem (N = 7168, K = 2048) timed the same way, not
-   part of `value` (--no-other-workloads skips it).
+   the other four workloads timed the same way, not part of `value`
+   (--no-other-workloads skips them).
+ * Outside the timed region: `prepack` (every SFA and SFB of the workload through
+   nvfp4_prepack_scales_batch, one launch, L2 flushed before each call, with its
+   bytes and roofline fraction) and `cold_call` (calls that miss the table cache,
+   against calls that hit it).
+ * `clocks`: SM clock, power and clock-event reasons of the GPU in use, sampled
+   every 5 ms through NVML during the timed region.
  * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
    scaling; the path has no exchange step). Timing is the max over ranks, and
    `value` = that time divided by N (aggregate time per grouped call).
@@ -122,61 +128,131 @@ def profiled_traffic(kernel, workload):
         return None
 
 
+def gpu_pci_id(local_rank):
+    """The PCI bus id of the CUDA device in use ("dddddddd:bb:dd.0"), which names the same GPU
+    to NVML and nvidia-smi whatever CUDA_VISIBLE_DEVICES maps; None where torch lacks it."""
+    import torch
+    p = torch.cuda.get_device_properties(local_rank)
+    try:
+        return "%08x:%02x:%02x.0" % (p.pci_domain_id, p.pci_bus_id, p.pci_device_id)
+    except AttributeError:
+        return None
+
+
 class ClockSampler:
-    """nvidia-smi clock and throttle-reason samples every 200 ms while running."""
+    """SM clock, power and clock-event reasons of the GPU in use, sampled every few
+    milliseconds while running: through NVML (libnvidia-ml, read-only queries) where it
+    loads, else nvidia-smi every 200 ms. window_begin()/window_end() bracket the timed
+    region; the summary covers the samples inside it, or, where the region was shorter
+    than one period, the samples of the whole run (said in `window`)."""
 
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
-             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+    NVML_REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+                    0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
+    SMI_QUERY = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+                 "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+                 "clocks_event_reasons.sw_power_cap")
 
-    def __init__(self, gpu_index):
-        self.gpu_index = gpu_index
-        self.proc = None
-        self.lines = []
+    def __init__(self, pci_id, period_s=0.005):
+        self.pci_id = pci_id
+        self.period_s = period_s
+        self.samples = []  # (t, sm_mhz, max_mhz, power_w, [reasons])
+        self.source = None
+        self.windows = []
+        self._stop = threading.Event()
+        self._thread = None
+        self._proc = None
+
+    def _nvml(self):
+        import ctypes
+        lib = ctypes.CDLL("libnvidia-ml.so.1")
+        if lib.nvmlInit_v2() != 0:
+            raise OSError("nvmlInit failed")
+        h = ctypes.c_void_p()
+        if self.pci_id is None or lib.nvmlDeviceGetHandleByPciBusId_v2(self.pci_id.encode(), ctypes.byref(h)) != 0:
+            raise OSError("no NVML handle for the device")
+        get_reasons = getattr(lib, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+            lib.nvmlDeviceGetCurrentClocksThrottleReasons
+        clk, mx, pw, rs = ctypes.c_uint(), ctypes.c_uint(), ctypes.c_uint(), ctypes.c_ulonglong()
+
+        def read():
+            lib.nvmlDeviceGetClockInfo(h, 1, ctypes.byref(clk))      # NVML_CLOCK_SM
+            lib.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx))
+            lib.nvmlDeviceGetPowerUsage(h, ctypes.byref(pw))
+            get_reasons(h, ctypes.byref(rs))
+            names = [n for bit, n in self.NVML_REASONS.items() if rs.value & bit]
+            return float(clk.value), float(mx.value), pw.value / 1000.0, names
+        read()
+        return read
+
+    def _loop(self, read):
+        while not self._stop.is_set():
+            try:
+                self.samples.append((time.perf_counter(),) + read())
+            except Exception:
+                pass
+            self._stop.wait(self.period_s)
+
+    def _smi_loop(self):
+        for line in self._proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                names = [n for n, v in zip(["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                            "sw_power_cap"], parts[3:7]) if v.lower() == "active"]
+                self.samples.append((time.perf_counter(), float(parts[0]), float(parts[1]), float(parts[2]), names))
+            except ValueError:
+                continue
 
     def __enter__(self):
         try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.QUERY}", "--format=csv,noheader,nounits",
-                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
-            self.thread.start()
+            read = self._nvml()
+            self.source = "nvml"
+            self._thread = threading.Thread(target=self._loop, args=(read,), daemon=True)
         except OSError:
-            self.proc = None
+            try:
+                cmd = ["nvidia-smi", f"--query-gpu={self.SMI_QUERY}", "--format=csv,noheader,nounits", "-lms", "200"]
+                if self.pci_id:
+                    cmd[1:1] = ["-i", self.pci_id]
+                self._proc = subprocess.Popen(cmd, stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+                self.source = "nvidia-smi"
+                self._thread = threading.Thread(target=self._smi_loop, daemon=True)
+            except OSError:
+                self._thread = None
+        if self._thread is not None:
+            self._thread.start()
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            self.lines.append(line.strip())
+    def window_begin(self):
+        self.windows.append([time.perf_counter(), None])
+
+    def window_end(self):
+        if self.windows:
+            self.windows[-1][1] = time.perf_counter()
 
     def __exit__(self, *exc):
-        if self.proc is not None:
-            self.proc.terminate()
+        self._stop.set()
+        if self._proc is not None:
+            self._proc.terminate()
             try:
-                self.proc.wait(timeout=5)
+                self._proc.wait(timeout=5)
             except subprocess.TimeoutExpired:
-                self.proc.kill()
-            self.thread.join(timeout=2)
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=2)
 
     def summary(self):
-        sm, smax, reasons = [], [], set()
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in self.lines:
-            parts = [p.strip() for p in line.split(",")]
-            if len(parts) < 9:
-                continue
-            try:
-                sm.append(float(parts[1]))
-                smax.append(float(parts[2]))
-            except ValueError:
-                continue
-            for name, val in zip(names, parts[5:9]):
-                if val.lower() == "active":
-                    reasons.add(name)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm)}
+        inside = [x for x in self.samples if any(a <= x[0] <= (b or a) for a, b in self.windows)]
+        window = "timed region"
+        if not inside:
+            inside, window = list(self.samples), "whole run (the timed region was shorter than one sample period)"
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0, "source": self.source}
+        reasons = sorted({n for x in inside for n in x[4]})
+        return {"sm_mhz": statistics.median(x[1] for x in inside), "sm_max_mhz": max(x[2] for x in inside),
+                "power_w_max": round(max(x[3] for x in inside), 1), "reasons": reasons, "samples": len(inside),
+                "window": window, "source": self.source, "period_ms": (self.period_s * 1e3 if self.source == "nvml"
+                                                                      else 200), "gpu_pci": self.pci_id}
 
 
 # --------------------------------------------------------- distributed glue --
@@ -254,7 +330,93 @@ def time_oracle(groups, target_s, threads):
 
 # ---------------------------------------------------------------- our arm ---
 
+def time_prepack(groups, dev, stream, flush, steps, peaks):
+    """nvfp4_prepack_scales_batch over every SFA and SFB of the workload (one launch), L2
+    flushed before each call, CUDA events around it. The result must equal the per-operand
+    prepack's bit for bit."""
+    import torch
+    import block_scaled_fp4_persistent_gb300 as nv
+    srcs, dsts, rows, Ks, singles = [], [], [], [], []
+    for g in groups:
+        for sf, r in ((g.SFA, g.M), (g.SFB, g.N)):
+            t = torch.from_numpy(np.ascontiguousarray(sf)).to(dev)
+            srcs.append(t)
+            dsts.append(torch.empty(max(1, nv.nvfp4_prepacked_scale_bytes(r, g.K)), dtype=torch.uint8, device=dev))
+            rows.append(r)
+            Ks.append(g.K)
+            singles.append(nv.prepack_scales(t, g.K))
+    args = ([t.data_ptr() for t in srcs], rows, Ks, [t.data_ptr() for t in dsts])
+    for _ in range(3):
+        flush()
+        nv.nvfp4_prepack_scales_batch(*args, stream)
+    torch.cuda.synchronize()
+    for a, b in zip(dsts, singles):
+        if not torch.equal(a, b):
+            raise RuntimeError("batched prepack differs from the per-operand prepack")
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev:
+        flush()
+        e0.record(stream)
+        nv.nvfp4_prepack_scales_batch(*args, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    us = statistics.fmean(a.elapsed_time(b) for a, b in ev) * 1e3
+    read = sum(r * k // 16 for r, k in zip(rows, Ks))
+    written = sum(nv.nvfp4_prepacked_scale_bytes(r, k) for r, k in zip(rows, Ks))
+    gbs = (read + written) / (us * 1e-6) / 1e9
+    return {"value": round(us, 3), "unit": "us", "steps": steps, "operands": len(rows), "launches": 1,
+            "algorithmic_bytes": read + written, "read_bytes": read, "written_bytes": written,
+            "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
+            "what": "nvfp4_prepack_scales_batch of every SFA and SFB of the workload, L2 flushed before each call"}
+
+
+def time_cold_calls(keep, stream, flush, reps):
+    """Calls that miss the table cache (each with a fresh C buffer, so a new table is built:
+    tensor maps encoded, tile lists built, table uploaded) against calls that hit it: host time
+    until the call returns, and event time of the call on the stream (upload included)."""
+    import torch
+    import block_scaled_fp4_persistent_gb300 as nv
+
+    def probs_with(Cs):
+        return [nv.problem(A, B, SFA, SFB, C) for (A, B, SFA, SFB, _), C in zip(keep, Cs)]
+
+    out = {}
+    alive = []  # every C of the misses stays allocated, so no pointer (and no table key) repeats
+    for kind in ("miss", "hit"):
+        fixed = [torch.empty_like(k[4]) for k in keep]
+        host, gpu = [], []
+        for i in range(reps):
+            Cs = [torch.empty_like(k[4]) for k in keep] if kind == "miss" else fixed
+            alive.append(Cs)
+            probs = probs_with(Cs)
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            t0 = time.perf_counter()
+            nv.nvfp4_grouped_gemm(probs, stream)
+            host.append((time.perf_counter() - t0) * 1e6)
+            e1.record(stream)
+            torch.cuda.synchronize()
+            if kind == "hit" and i == 0:
+                host.clear()  # the first call of the fixed set is itself a miss
+                continue
+            gpu.append(e0.elapsed_time(e1) * 1e3)
+        out[kind] = {"host_us": round(statistics.median(host), 1), "gpu_us": round(statistics.median(gpu), 3)}
+    out["reps"] = reps
+    out["what"] = ("miss: every call with a new C pointer builds and uploads a new table (the cache holds 32, so "
+                   "misses also evict); hit: the same call repeated. host_us = time until the call returns; "
+                   "gpu_us = event time on the stream (table upload and kernel), L2 flushed before each call")
+    return out
+
+
 def run_ours(args, groups, rank, world, local_rank):
+    import torch
+    import block_scaled_fp4_persistent_gb300 as nv
+    with ClockSampler(gpu_pci_id(local_rank)) as clocks:
+        return _run_ours(args, groups, rank, world, local_rank, clocks)
+
+
+def _run_ours(args, groups, rank, world, local_rank, clocks):
     import torch
     import block_scaled_fp4_persistent_gb300 as nv
 
@@ -295,19 +457,20 @@ def run_ours(args, groups, rank, world, local_rank):
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     fl_starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local_rank) as clocks:
-        barrier(world)
-        torch.cuda.synchronize()
-        w0 = time.perf_counter()
-        for i in range(args.steps):
-            fl_starts[i].record(stream)
-            flush()
-            starts[i].record(stream)
-            nv.nvfp4_grouped_gemm(probs, stream)
-            ends[i].record(stream)
-        torch.cuda.synchronize()
-        barrier(world)
-        wall = time.perf_counter() - w0
+    barrier(world)
+    torch.cuda.synchronize()
+    clocks.window_begin()
+    w0 = time.perf_counter()
+    for i in range(args.steps):
+        fl_starts[i].record(stream)
+        flush()
+        starts[i].record(stream)
+        nv.nvfp4_grouped_gemm(probs, stream)
+        ends[i].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    wall = time.perf_counter() - w0
+    clocks.window_end()
     st, detail = nv.nvfp4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
@@ -417,6 +580,10 @@ def run_ours(args, groups, rank, world, local_rank):
         if not torch.equal(C.cpu().view(torch.int16), hC):
             raise RuntimeError("e2e output differs from the resident-input output")
 
+    # outside the timed region: the prepack on its own, and table-cache misses
+    prepack = time_prepack(groups, dev, stream, flush, min(args.steps, 200), peaks)
+    cold = time_cold_calls(keep, stream, flush, 40)
+
     achieved_gbs = nbytes / (mean_us * 1e-6) / 1e9
     roof_us = max(t_fp4_us, t_hbm_us)
     out = {
@@ -459,6 +626,8 @@ def run_ours(args, groups, rank, world, local_rank):
                        "l2_flush": round(sum(flush_ms) / (sum(per_call_ms) + sum(flush_ms)), 4)},
         "timed_region_wall_s": round(wall, 3),
         "clocks": clocks.summary(),
+        "prepack": prepack,
+        "cold_call": cold,
         "chained": {"value": round(chain_us / world, 3), "unit": "us", "calls_per_batch": chain_calls,
                     "batches": chain_batches, "pdl": True,
                     "l2": ("flushed before each batch only; one call's inputs and C (%.0f MB) %s L2 (%.0f MB)"
@@ -582,16 +751,20 @@ def main():
     groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
     out = run_ours(args, groups, rank, world, local_rank)
     if world == 1 and args.workload == "moe_g8_n4096_k7168" and not args.no_other_workloads:
-        # the other MoE-shaped workload, timed the same way (not part of the headline value)
-        other = "moe_g8_n7168_k2048"
-        other_groups = gen.make_workload(other)
-        us, kern = time_flushed(other_groups, min(args.steps, 2000), args.warmup, local_rank)
+        # the other workloads, timed the same way (not part of the headline value)
+        out["other_workloads"] = {}
         peaks, _ = load_peaks()
-        _, _, _, t_fp4, t_hbm = roofline_terms(other_groups, peaks)
-        out["other_workloads"] = {other: {"value": round(us, 3), "unit": "us", "steps": min(args.steps, 2000),
-                                          "roofline_fraction": round(max(t_fp4, t_hbm) / us, 4), "kernel": kern,
-                                          "vs_baseline": round(us / PAGES_BEST_US[other], 4),
-                                          "l2": "flushed before every timed call"}}
+        for other in ("moe_g8_n7168_k2048", "g2_n3072_k4096", "g2_n4096_k1536", "tiny_g2"):
+            other_groups = gen.make_workload(other)
+            steps = min(args.steps, 2000)
+            us, kern = time_flushed(other_groups, steps, args.warmup, local_rank)
+            _, nb, _, t_fp4, t_hbm = roofline_terms(other_groups, peaks)
+            out["other_workloads"][other] = {
+                "value": round(us, 3), "unit": "us", "steps": steps,
+                "roofline_fraction": round(max(t_fp4, t_hbm) / us, 4),
+                "tbs": round(nb / (us * 1e-6) / 1e12, 4), "kernel": kern,
+                "vs_baseline": round(us / PAGES_BEST_US[other], 4) if other in PAGES_BEST_US else None,
+                "l2": "flushed before every timed call"}
     if rank == 0:
         if not args.no_cpu_baseline:
             threads = os.cpu_count() or 1

@@ -8,11 +8,11 @@ been built, the first call raises ImportError. Build it with
 ``block_scaled_fp4_persistent_gb300._build.build()`` or
 ``__graft_entry__.build()``.
 
-Names match the C ABI: ``nvfp4_grouped_gemm``, ``nvfp4_prepack_scales``,
+Names match the C ABI: ``nvfp4_grouped_gemm``, ``nvfp4_prepack_scales``, ``nvfp4_prepack_scales_batch``,
 ``nvfp4_prepacked_scale_bytes``, ``nvfp4_device_status``,
 ``nvfp4_status_string``, ``nvfp4_last_cuda_error``, ``nvfp4_last_kernel``, ``nvfp4_last_launches``,
-``nvfp4_last_a_maps``, ``nvfp4_set_option`` and
-``nvfp4_release``.
+``nvfp4_last_a_maps``, ``nvfp4_set_option``, ``nvfp4_release``,
+``nvfp4_grouped_gemm_noalloc`` and ``nvfp4_noalloc_status``.
 """
 from __future__ import annotations
 
@@ -30,6 +30,7 @@ NVFP4_ERR_UNSUPPORTED_DEVICE = -3
 NVFP4_ERR_CUDA = -4
 NVFP4_ERR_TIMEOUT = -5
 NVFP4_ERR_TOO_LARGE = -6
+NVFP4_ERR_CAPTURE = -7
 
 NVFP4_SF_PREPACKED = 0
 NVFP4_SF_ROWMAJOR = 1
@@ -78,6 +79,10 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_prepacked_scale_bytes.argtypes = [ctypes.c_int, ctypes.c_int]
     lib.nvfp4_prepack_scales.restype = ctypes.c_int
     lib.nvfp4_prepack_scales.argtypes = [ctypes.c_void_p, ctypes.c_int, ctypes.c_int, ctypes.c_void_p, ctypes.c_void_p]
+    lib.nvfp4_prepack_scales_batch.restype = ctypes.c_int
+    lib.nvfp4_prepack_scales_batch.argtypes = [ctypes.c_int, ctypes.POINTER(ctypes.c_void_p),
+                                               ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int),
+                                               ctypes.POINTER(ctypes.c_void_p), ctypes.c_void_p]
     lib.nvfp4_device_status.restype = ctypes.c_int
     lib.nvfp4_device_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int32)]
     lib.nvfp4_status_string.restype = ctypes.c_char_p
@@ -94,6 +99,10 @@ def _load() -> ctypes.CDLL:
     lib.nvfp4_set_option.argtypes = [ctypes.c_int, ctypes.c_int64]
     lib.nvfp4_release.restype = None
     lib.nvfp4_release.argtypes = []
+    lib.nvfp4_grouped_gemm_noalloc.restype = ctypes.c_int
+    lib.nvfp4_grouped_gemm_noalloc.argtypes = [ctypes.c_int, ctypes.POINTER(Nvfp4Problem), ctypes.c_void_p]
+    lib.nvfp4_noalloc_status.restype = ctypes.c_int
+    lib.nvfp4_noalloc_status.argtypes = [ctypes.c_void_p, ctypes.POINTER(ctypes.c_int), ctypes.POINTER(ctypes.c_int32)]
     return lib
 
 
@@ -147,6 +156,21 @@ def nvfp4_prepack_scales(sf_rowmajor_ptr: int, rows: int, K: int, sf_blocked_ptr
                          check: bool = True) -> int:
     rc = _get().nvfp4_prepack_scales(sf_rowmajor_ptr, rows, K, sf_blocked_ptr, _stream_handle(stream))
     return _check(rc, "nvfp4_prepack_scales") if check else rc
+
+
+def nvfp4_prepack_scales_batch(src_ptrs: Sequence[int], rows: Sequence[int], Ks: Sequence[int],
+                               dst_ptrs: Sequence[int], stream=None, check: bool = True) -> int:
+    """Prepack of several operands in one launch (see the C header)."""
+    n = len(src_ptrs)
+    if not (len(rows) == len(Ks) == len(dst_ptrs) == n):
+        raise ValueError("nvfp4_prepack_scales_batch: the four lists must have the same length")
+    m = max(1, n)
+    src = (ctypes.c_void_p * m)(*src_ptrs)
+    dst = (ctypes.c_void_p * m)(*dst_ptrs)
+    r = (ctypes.c_int * m)(*rows)
+    k = (ctypes.c_int * m)(*Ks)
+    rc = _get().nvfp4_prepack_scales_batch(n, src, r, k, dst, _stream_handle(stream))
+    return _check(rc, "nvfp4_prepack_scales_batch") if check else rc
 
 
 def nvfp4_device_status(stream=None) -> Tuple[int, List[int]]:
@@ -210,10 +234,14 @@ def prepack_scales(sf_rowmajor, K: int, out=None, stream=None):
 def nvfp4_grouped_gemm_noalloc(probs: Sequence[Nvfp4Problem], stream=None, check: bool = True) -> int:
     """The grouped GEMM without any device allocation: its problem table lives in a
     fixed 256 KB array inside the library (see the C header for the limits)."""
-    lib_ = _get()
-    fn = lib_.nvfp4_grouped_gemm_noalloc
-    fn.restype = ctypes.c_int
-    fn.argtypes = [ctypes.c_int, ctypes.POINTER(Nvfp4Problem), ctypes.c_void_p]
     arr = (Nvfp4Problem * max(1, len(probs)))(*probs)
-    rc = fn(len(probs), arr, _stream_handle(stream))
+    rc = _get().nvfp4_grouped_gemm_noalloc(len(probs), arr, _stream_handle(stream))
     return _check(rc, "nvfp4_grouped_gemm_noalloc") if check else rc
+
+
+def nvfp4_noalloc_status(stream=None) -> Tuple[int, List[int]]:
+    """(status, [code, role, item, stage]) of the no-allocation kernel's error words; reading clears them."""
+    st = ctypes.c_int(0)
+    detail = (ctypes.c_int32 * 4)()
+    _check(_get().nvfp4_noalloc_status(_stream_handle(stream), ctypes.byref(st), detail), "nvfp4_noalloc_status")
+    return st.value, list(detail)

@@ -380,6 +380,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
             struct Src {  // where one tile's stages come from
+                int group;
                 const void *tmap_a, *tmap_b;
                 int32_t ya, yb;
                 int kb64, kb_begin, kb_end;
@@ -394,6 +395,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 Src r;
                 const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: no load
+                r.group = w.group;
                 r.tmap_a = &ge.tmap_a;  // one A map per group: M-fusion is for CTA pairs only
                 r.tmap_b = &ge.tmap_b;
                 r.ya = w.tile_m * kBlockM;
@@ -414,6 +416,21 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     r.sfb[L::kHalves - 1] = w.sfb + ((w.flags & kItemB2) ? (size_t)r.kb64 * kScaleBlockBytes : 0);
                 return r;
             };
+            // Before this thread's first copy (or prefetch) through a group's maps, the
+            // acquire fence for each of them (see tensormap_acquire). Items come group by
+            // group, so this runs about once per group.
+            int fenced = -1;
+            auto acquire_maps = [&](const Src &s) {
+                if (s.group == fenced)
+                    return;
+                fenced = s.group;
+                tensormap_acquire(s.tmap_a);
+                tensormap_acquire(s.tmap_b);
+                if (s.sf_rowmajor) {
+                    tensormap_acquire(s.tmap_sfa);
+                    tensormap_acquire(s.tmap_sfb);
+                }
+            };
             // prefetch cursor
             uint32_t pf_it = item_begin, pf_g = 0;
             Src pf{};
@@ -422,6 +439,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             int pf_kb = pf.kb_begin;
             auto prefetch_until = [&](uint32_t g_end) {
                 while (pf_g < g_end && pf_it < item_end) {
+                    acquire_maps(pf);
                     const uint32_t sfb_bytes = (uint32_t)min(4, pf.kb64 - pf_kb * 4) * kScaleBlockBytes;
                     tma_prefetch_2d(pf.tmap_a, pf_kb * kRowBytes, pf.ya);
                     tma_prefetch_2d(pf.tmap_b, pf_kb * kRowBytes, pf.yb);
@@ -448,6 +466,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const Src src = source(it);
+                acquire_maps(src);
                 const uint64_t pol_b = src.b_shared ? pol_b_shared : pol_b_stream;
                 for (int kb = src.kb_begin; kb < src.kb_end; ++kb, ++kiter) {
                     if (pf_dist > 0)
@@ -609,11 +628,16 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
+        int fenced = -1;  // the group whose C map lane 0 last fenced (it issues the stores)
         grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
+            if (lane == 0 && w.group != fenced) {
+                tensormap_acquire(&ge.tmap_c);
+                fenced = w.group;
+            }
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
                 break;
             acc_phase ^= 1u;

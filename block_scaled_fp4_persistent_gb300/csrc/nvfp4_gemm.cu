@@ -110,6 +110,27 @@ struct DeviceState {
 std::mutex g_mu;  // guards everything below
 DeviceState g_dev[kMaxDevices];
 
+// The memory behind one cached table: the device table, its pinned host copy (the
+// source of the asynchronous upload), and for split schedules the fp32 workspace
+// and the counters. Blocks are recycled through a per-device pool rather than
+// freed, and a block leaves a table only once the work that may read it has
+// completed: each stream that launched with the table records an event after the
+// launch, and an evicted table's blocks wait in a retiring list until all its
+// events have completed. Nothing synchronises.
+struct Buffers {
+    int device = -1;
+    void *dev = nullptr;
+    size_t dev_cap = 0;
+    void *host = nullptr;
+    size_t host_cap = 0;
+    float *ws = nullptr;
+    size_t ws_cap = 0;
+    int *cnt = nullptr;
+    size_t cnt_cap = 0;
+    std::vector<std::pair<cudaStream_t, cudaEvent_t>> uses;  // one event per stream that used the blocks
+    bool untracked = false;  // more streams than tracked: retire only after a device synchronisation
+};
+
 struct CachedTable {
     uint64_t key = 0;
     std::vector<uint8_t> signature;  // exact inputs of the table, to rule out hash collisions
@@ -124,7 +145,9 @@ struct CachedTable {
     int block_n = 0;
     int variant = 0;  // the kernel variant the table was built for
     int a_maps = 0;   // distinct A tensor maps: one per run of groups with consecutive A rows
+    bool captured = false;  // used inside a stream capture: a graph may replay it, so it is never evicted
     std::vector<uint32_t> list_begin;  // the table's cta_begin, passed again with each launch
+    Buffers buf;
 };
 // The device address of a cached table's work items.
 const int4 *table_items(const CachedTable &t)
@@ -135,7 +158,6 @@ const int4 *table_items(const CachedTable &t)
 
 std::list<CachedTable> g_tables;  // most recently used first
 std::unordered_map<uint64_t, std::list<CachedTable>::iterator> g_table_index;
-
 struct Workspace {
     void *ptr = nullptr;
     size_t bytes = 0;
@@ -156,6 +178,150 @@ int cuda_fail(cudaError_t e)
         if (e_ != cudaSuccess)                  \
             return cuda_fail(e_);               \
     } while (0)
+
+std::vector<Buffers> g_free_buffers;      // blocks that no queued work reads any more
+std::vector<Buffers> g_retiring_buffers;  // blocks of evicted tables, waiting for their events
+constexpr size_t kMaxFreeBuffers = 16;    // beyond this, idle blocks are returned to CUDA
+
+size_t pool_round(size_t n) { return n == 0 ? 0 : std::max<size_t>(16384, size_t(1) << (64 - __builtin_clzll(n - 1))); }
+
+void free_buffers(Buffers &b)
+{
+    for (auto &u : b.uses)
+        cudaEventDestroy(u.second);
+    b.uses.clear();
+    cudaFree(b.dev);
+    cudaFree(b.ws);
+    cudaFree(b.cnt);
+    cudaFreeHost(b.host);
+    b = Buffers{};
+}
+
+// Whether every event of b has completed (nothing queued reads the blocks).
+bool buffers_idle(const Buffers &b)
+{
+    if (b.untracked)
+        return false;
+    for (const auto &u : b.uses) {
+        cudaError_t q = cudaEventQuery(u.second);
+        if (q == cudaErrorNotReady)
+            return false;
+        if (q != cudaSuccess)
+            cudaGetLastError();  // a failed event is not waited for: clear the sticky error
+    }
+    return true;
+}
+
+// Blocks of at least the given sizes on device dev: a free block of the pool that
+// fits (the smallest), else new ones with sizes rounded up to powers of two.
+int acquire_buffers(int dev, size_t table_bytes, size_t ws_bytes, size_t cnt_bytes, Buffers *out)
+{
+    for (size_t i = 0; i < g_retiring_buffers.size();) {
+        if (buffers_idle(g_retiring_buffers[i])) {
+            g_free_buffers.push_back(std::move(g_retiring_buffers[i]));
+            g_retiring_buffers.erase(g_retiring_buffers.begin() + i);
+        } else {
+            ++i;
+        }
+    }
+    int best = -1;
+    size_t best_size = SIZE_MAX;
+    for (size_t i = 0; i < g_free_buffers.size(); ++i) {
+        const Buffers &b = g_free_buffers[i];
+        if (b.device != dev || b.dev_cap < table_bytes || b.host_cap < table_bytes || b.ws_cap < ws_bytes ||
+            b.cnt_cap < cnt_bytes)
+            continue;
+        const size_t sz = b.dev_cap + b.ws_cap + b.cnt_cap;
+        if (sz < best_size) {
+            best_size = sz;
+            best = (int)i;
+        }
+    }
+    if (best >= 0) {
+        *out = std::move(g_free_buffers[best]);
+        g_free_buffers.erase(g_free_buffers.begin() + best);
+        return NVFP4_OK;
+    }
+    Buffers b;
+    b.device = dev;
+    b.dev_cap = b.host_cap = pool_round(table_bytes);
+    b.ws_cap = pool_round(ws_bytes);
+    b.cnt_cap = pool_round(cnt_bytes);
+    cudaError_t e = cudaMalloc(&b.dev, b.dev_cap);
+    if (e == cudaSuccess)
+        e = cudaMallocHost(&b.host, b.host_cap);
+    if (e == cudaSuccess && b.ws_cap)
+        e = cudaMalloc(&b.ws, b.ws_cap);
+    if (e == cudaSuccess && b.cnt_cap)
+        e = cudaMalloc(&b.cnt, b.cnt_cap);
+    if (e != cudaSuccess) {
+        free_buffers(b);
+        return cuda_fail(e);
+    }
+    *out = std::move(b);
+    return NVFP4_OK;
+}
+
+// Blocks that no queued work has touched yet (the table was never uploaded) go
+// straight back to the pool; the others wait for their events.
+void return_buffers(Buffers &&b, bool used)
+{
+    if (used) {
+        g_retiring_buffers.push_back(std::move(b));
+    } else {
+        g_free_buffers.push_back(std::move(b));
+    }
+    while (g_free_buffers.size() > kMaxFreeBuffers) {
+        free_buffers(g_free_buffers.front());
+        g_free_buffers.erase(g_free_buffers.begin());
+    }
+}
+
+// After queuing work that reads t's blocks on `stream`: record (or re-record) the
+// stream's event. Inside a stream capture the table is marked captured instead:
+// a graph may replay the work at any later time, so the table stays cached.
+int note_use(CachedTable &t, cudaStream_t stream)
+{
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+    if (cs != cudaStreamCaptureStatusNone) {
+        t.captured = true;
+        return NVFP4_OK;
+    }
+    for (auto &u : t.buf.uses)
+        if (u.first == stream) {
+            CUDA_TRY(cudaEventRecord(u.second, stream));
+            return NVFP4_OK;
+        }
+    if (t.buf.uses.size() >= 16) {
+        t.buf.untracked = true;
+        return NVFP4_OK;
+    }
+    cudaEvent_t ev = nullptr;
+    CUDA_TRY(cudaEventCreateWithFlags(&ev, cudaEventDisableTiming));
+    t.buf.uses.push_back({stream, ev});
+    CUDA_TRY(cudaEventRecord(ev, stream));
+    return NVFP4_OK;
+}
+
+// Takes a table out of the cache; its blocks retire once their events complete.
+void evict_table(std::list<CachedTable>::iterator it)
+{
+    auto idx = g_table_index.find(it->key);
+    if (idx != g_table_index.end() && idx->second == it)
+        g_table_index.erase(idx);
+    if (it->buf.untracked) {
+        // more streams used it than are tracked: wait for the device once
+        cudaDeviceSynchronize();
+        it->buf.untracked = false;
+        for (auto &u : it->buf.uses)
+            cudaEventDestroy(u.second);
+        it->buf.uses.clear();
+    }
+    return_buffers(std::move(it->buf), true);
+    g_tables.erase(it);
+}
+
 
 uint64_t fnv1a(const void *data, size_t n, uint64_t h = 1469598103934665603ull)
 {
@@ -559,6 +725,11 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         *out = &g_tables.front();
         return NVFP4_OK;
     }
+    if (it != g_table_index.end() && !it->second->captured) {
+        // a hash collision: the older table leaves the cache, the new one takes its key
+        evict_table(it->second);
+        it = g_table_index.end();
+    }
     if (int rc = get_encoder())
         return rc;
 
@@ -596,7 +767,14 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     t.variant = variant;
     t.a_maps = runs.maps;
     t.list_begin = sc.list_begin;
-    CUDA_TRY(cudaMallocHost(&t.host, total));
+    const size_t ws_bytes = sc.splits > 0 ? (size_t)sc.ws_slots * halves * kBlockM * block_n * sizeof(float) : 0;
+    const size_t cnt_bytes = sc.splits > 0 ? (size_t)sc.splits * halves * sizeof(int) : 0;
+    if (int rc = acquire_buffers(dev, total, ws_bytes, cnt_bytes, &t.buf))
+        return rc;
+    t.host = t.buf.host;
+    t.dev = t.buf.dev;
+    t.workspace = sc.splits > 0 ? t.buf.ws : nullptr;
+    t.counters = sc.splits > 0 ? t.buf.cnt : nullptr;
     memset(t.host, 0, total);
     uint8_t *h = static_cast<uint8_t *>(t.host);
     TableHeader *th = reinterpret_cast<TableHeader *>(h);
@@ -637,7 +815,7 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
                                                   pair ? (uint32_t)kPairBlockN : (uint32_t)block_n)
                                : encode_unused_scale_map(&e.tmap_sfb, a.SFB);
         if (rc) {
-            cudaFreeHost(t.host);
+            return_buffers(std::move(t.buf), false);
             return rc;
         }
         e.sfa = static_cast<const uint8_t *>(a.SFA);
@@ -655,45 +833,34 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     if (!items.empty())
         memcpy(h + off_items, items.data(), items.size() * sizeof(WorkItem));
 
-    cudaError_t e = cudaMalloc(&t.dev, total);
-    if (e != cudaSuccess) {
-        cudaFreeHost(t.host);
-        return cuda_fail(e);
-    }
-    e = cudaMemcpyAsync(t.dev, t.host, total, cudaMemcpyHostToDevice, stream);
+    cudaError_t e = cudaMemcpyAsync(t.dev, t.host, total, cudaMemcpyHostToDevice, stream);
     if (e == cudaSuccess && sc.splits > 0) {
-        e = cudaMalloc(&t.workspace, (size_t)sc.ws_slots * halves * kBlockM * block_n * sizeof(float));
-        if (e == cudaSuccess)
-            e = cudaMalloc(&t.counters, (size_t)sc.splits * halves * sizeof(int));
-        if (e == cudaSuccess)
-            e = cudaMemsetAsync(t.counters, 0, (size_t)sc.splits * halves * sizeof(int), stream);
+        e = cudaMemsetAsync(t.counters, 0, cnt_bytes, stream);
         t.splits = sc.splits * halves;
     }
     if (e != cudaSuccess) {
-        cudaFree(t.dev);
-        cudaFree(t.workspace);
-        cudaFree(t.counters);
-        cudaFreeHost(t.host);
+        return_buffers(std::move(t.buf), true);
         return cuda_fail(e);
     }
 
+    // The least recently used table leaves (tables a graph may replay stay); its
+    // blocks retire once the work queued with them has completed.
     if (g_tables.size() >= kMaxCachedTables) {
-        // The oldest table may still be read by queued work on any stream.
-        CUDA_TRY(cudaDeviceSynchronize());
-        CachedTable &old = g_tables.back();
-        cudaFree(old.dev);
-        cudaFree(old.workspace);
-        cudaFree(old.counters);
-        cudaFreeHost(old.host);
-        g_table_index.erase(old.key);
-        g_tables.pop_back();
+        for (auto old = g_tables.end(); old != g_tables.begin();) {
+            --old;
+            if (!old->captured) {
+                evict_table(old);
+                break;
+            }
+        }
     }
-    if (it != g_table_index.end())
-        g_table_index.erase(it);  // a hash collision: the newer table takes the slot
     g_tables.push_front(std::move(t));
+    if (it != g_table_index.end())
+        g_table_index.erase(it);  // a collision with a captured table: the newer one takes the key
     g_table_index[key] = g_tables.begin();
     *out = &g_tables.front();
-    return NVFP4_OK;
+    // the upload reads the pinned copy: its blocks are in use from here on
+    return note_use(g_tables.front(), stream);
 }
 
 // Sets the kernel's shared-memory limit once per device and checks that one CTA
@@ -914,6 +1081,7 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     if (rc == NVFP4_OK) {
         g_last_launches.store(prepack_launches + 1);
         g_last_a_maps.store(t->a_maps);
+        rc = note_use(*t, stream);
     }
     return rc;
 }
@@ -947,6 +1115,45 @@ extern "C" int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, vo
     }
     PrepackJob j{static_cast<const uint8_t *>(sf_rowmajor), static_cast<uint8_t *>(sf_blocked), rows, K / 16, 0, 0, 0};
     CUDA_TRY(launch_prepack(&j, 1, reinterpret_cast<cudaStream_t>(stream)));
+    return NVFP4_OK;
+}
+
+extern "C" int nvfp4_prepack_scales_batch(int n, const void *const *sf_rowmajor, const int *rows, const int *K,
+                                          void *const *sf_blocked, nvfp4_stream_t stream)
+{
+    if (n < 0)
+        return NVFP4_ERR_INVALID_ARG;
+    if (n == 0)
+        return NVFP4_OK;
+    if (!sf_rowmajor || !rows || !K || !sf_blocked)
+        return NVFP4_ERR_INVALID_ARG;
+    std::vector<PrepackJob> jobs;
+    jobs.reserve(n);
+    for (int i = 0; i < n; ++i) {
+        if (rows[i] < 0 || K[i] < 0 || K[i] % 16 != 0)
+            return NVFP4_ERR_INVALID_ARG;
+        if (rows[i] >= kMaxDim || K[i] >= kMaxDim)
+            return NVFP4_ERR_TOO_LARGE;
+        if (rows[i] == 0 || K[i] == 0)
+            continue;
+        if (!sf_rowmajor[i] || !sf_blocked[i])
+            return NVFP4_ERR_INVALID_ARG;
+        if (!aligned16(sf_rowmajor[i]) || !aligned16(sf_blocked[i]))
+            return NVFP4_ERR_ALIGNMENT;
+        jobs.push_back(PrepackJob{static_cast<const uint8_t *>(sf_rowmajor[i]), static_cast<uint8_t *>(sf_blocked[i]),
+                                  rows[i], K[i] / 16, 0, 0, 0});
+    }
+    if (jobs.empty())
+        return NVFP4_OK;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        int dev = 0;
+        CUDA_TRY(cudaGetDevice(&dev));
+        DeviceState *ds = nullptr;
+        if (int rc = device_state(dev, &ds))
+            return rc;
+    }
+    CUDA_TRY(launch_prepack(jobs.data(), (int)jobs.size(), reinterpret_cast<cudaStream_t>(stream)));
     return NVFP4_OK;
 }
 
@@ -987,6 +1194,7 @@ extern "C" const char *nvfp4_status_string(int code)
     case NVFP4_ERR_CUDA: return "CUDA error (see nvfp4_last_cuda_error)";
     case NVFP4_ERR_TIMEOUT: return "a kernel wait timed out";
     case NVFP4_ERR_TOO_LARGE: return "size beyond the library's limits";
+    case NVFP4_ERR_CAPTURE: return "not allowed while the stream is being captured";
     default: return "unknown status";
     }
 }
@@ -1075,16 +1283,24 @@ extern "C" void nvfp4_release(void)
         cudaDeviceSynchronize();
         for (auto it = g_tables.begin(); it != g_tables.end();) {
             if (it->device == d) {
-                cudaFree(it->dev);
-                cudaFree(it->workspace);
-                cudaFree(it->counters);
-                cudaFreeHost(it->host);
-                g_table_index.erase(it->key);
+                auto idx = g_table_index.find(it->key);
+                if (idx != g_table_index.end() && idx->second == it)
+                    g_table_index.erase(idx);
+                free_buffers(it->buf);
                 it = g_tables.erase(it);
             } else {
                 ++it;
             }
         }
+        for (std::vector<Buffers> *pool : {&g_free_buffers, &g_retiring_buffers})
+            for (auto it = pool->begin(); it != pool->end();) {
+                if (it->device == d) {
+                    free_buffers(*it);
+                    it = pool->erase(it);
+                } else {
+                    ++it;
+                }
+            }
         for (auto it = g_workspaces.begin(); it != g_workspaces.end();) {
             if (it->first.first == d) {
                 cudaFree(it->second.ptr);
@@ -1125,10 +1341,13 @@ extern "C" void nvfp4_release(void)
 //    without ordering between them) race on it and must not be issued.
 //  * The first call on a device does the set-up: the device checks, the
 //    cudaGetSymbolAddress lookup of the array and the kernel's shared-memory
-//    attribute. Make that first call before any stream capture.
-//  * The error words are cleared at the start of every call. A wait that runs
-//    out inside this kernel ends the launch early, but nvfp4_device_status
-//    does not see it.
+//    attribute.
+//  * A call on a stream that is being captured returns NVFP4_ERR_CAPTURE and
+//    queues nothing: the table copy would become a graph node that reads the
+//    static host buffer when the graph is replayed, by then another call's table.
+//  * The kernel's error words (the first 16 bytes of the array) are sticky: a
+//    wait that runs out records NVFP4_ERR_TIMEOUT there and ends the launch
+//    early. nvfp4_noalloc_status reads and clears them without allocating.
 
 namespace {
 
@@ -1183,6 +1402,12 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     cudaStream_t stream = reinterpret_cast<cudaStream_t>(stream_);
     if (g < 0)
         return NVFP4_ERR_INVALID_ARG;
+    {
+        cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+        CUDA_TRY(cudaStreamIsCapturing(stream, &cs));
+        if (cs != cudaStreamCaptureStatusNone)
+            return NVFP4_ERR_CAPTURE;
+    }
     if (g == 0)
         return NVFP4_OK;
     if (!probs)
@@ -1303,9 +1528,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     }
 
     uint8_t *dscratch = nd->scratch;
-    int *dstatus = reinterpret_cast<int *>(dscratch);
+    int *dstatus = reinterpret_cast<int *>(dscratch);  // sticky: cleared by nvfp4_noalloc_status
     const Table *dtable = reinterpret_cast<const Table *>(dscratch + kNoAllocStatusBytes);
-    CUDA_TRY(cudaMemsetAsync(dstatus, 0, kNoAllocStatusBytes, stream));
     // From pageable memory: returns once the bytes are staged, so the host
     // buffer may be reused by the next call.
     CUDA_TRY(cudaMemcpyAsync(dscratch + kNoAllocStatusBytes, h, total, cudaMemcpyHostToDevice, stream));
@@ -1315,7 +1539,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.items = reinterpret_cast<const int4 *>(reinterpret_cast<const uint8_t *>(dtable) + off_items);
     args.status = dstatus;
     args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
-    args.fault_skip_load = -1;
+    args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
     args.num_groups = (int32_t)ngroups;
     args.prefetch_stages = kDefaultPrefetchStages;
     args.workspace = nullptr;  // no split tiles here
@@ -1326,5 +1550,30 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");
     g_last_launches.store(1);
     g_last_a_maps.store(ngroups);  // no M-fusion here: one A map per group
+    return NVFP4_OK;
+}
+
+extern "C" int nvfp4_noalloc_status(nvfp4_stream_t stream, int *status, int32_t *detail)
+{
+    if (!status)
+        return NVFP4_ERR_INVALID_ARG;
+    std::lock_guard<std::mutex> lock(g_noalloc_mu);
+    int dev = 0;
+    CUDA_TRY(cudaGetDevice(&dev));
+    NoAllocDevice *nd = nullptr;
+    if (int rc = noalloc_setup(dev, &nd))
+        return rc;
+    CUDA_TRY(cudaStreamSynchronize(reinterpret_cast<cudaStream_t>(stream)));
+    int32_t words[4] = {0, 0, 0, 0};
+    // Reads and writes the array through its symbol: no device allocation.
+    CUDA_TRY(cudaMemcpyFromSymbol(words, g_noalloc_scratch, sizeof(words), 0, cudaMemcpyDeviceToHost));
+    if (words[0] != 0) {
+        const int32_t zero[4] = {0, 0, 0, 0};
+        CUDA_TRY(cudaMemcpyToSymbol(g_noalloc_scratch, zero, sizeof(zero), 0, cudaMemcpyHostToDevice));
+    }
+    *status = words[0];
+    if (detail)
+        for (int i = 0; i < 4; ++i)
+            detail[i] = words[i];
     return NVFP4_OK;
 }

@@ -155,11 +155,26 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             const uint64_t pol_b_stream = policy_evict_first();
             const uint64_t pol_b_shared = policy_evict_normal();
             uint32_t stage = 0, phase = 0, kiter = 0;
+            int fenced_b = -1, fenced_a = -1;  // groups whose maps this thread has fenced (tensormap_acquire)
             bool ok = true;
             for (uint32_t it = item_begin; ok && it < item_end; ++it) {
                 const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: the tensor maps
-                const GroupEntry &ga = tab->group(w.flags >> kItemAMapShift);  // the (possibly shared) A map
+                const int a_map = w.flags >> kItemAMapShift;
+                const GroupEntry &ga = tab->group(a_map);  // the (possibly shared) A map
+                const bool sf_rm_item = (w.flags & kItemSfRowMajor) != 0;
+                if (w.group != fenced_b) {
+                    fenced_b = w.group;
+                    tensormap_acquire(&ge.tmap_b);
+                    if (sf_rm_item)
+                        tensormap_acquire(&ge.tmap_sfb);
+                }
+                if (a_map != fenced_a) {
+                    fenced_a = a_map;
+                    tensormap_acquire(&ga.tmap_a);
+                    if (sf_rm_item)
+                        tensormap_acquire(&ga.tmap_sfa);
+                }
                 const int kb64 = w.kblocks64;
                 const int32_t ya = w.a_row + (int)rank * 128;
                 const int32_t yb = w.tile_n * kPairBlockN + (int)rank * 128;
@@ -332,11 +347,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
+        int fenced = -1;  // the group whose C map lane 0 last fenced (it issues the stores)
         grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
+            if (lane == 0 && w.group != fenced) {
+                tensormap_acquire(&ge.tmap_c);
+                fenced = w.group;
+            }
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
                 break;
             acc_phase ^= 1u;

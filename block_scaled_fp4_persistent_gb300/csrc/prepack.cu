@@ -9,11 +9,17 @@
 // A 512-byte block is exactly what one `tcgen05.cp .32x128b.warpx4` moves into
 // four TMEM columns.
 //
-// Work split. One CTA per (128-row tile, 8 column blocks). Its 256 threads first
-// load the 128 x 32-byte source tile into shared memory (reads coalesced along
-// each row). Then each thread writes one 16-byte row of a 512-byte block, so
-// consecutive threads write consecutive 16 bytes. The kernel moves bytes and
-// is bound by HBM bandwidth.
+// Work split. One CTA per (128-row tile, up to 128 source columns = 32 blocks),
+// for every operand of the launch. The kernel moves bytes and is bound by HBM
+// bandwidth, so both sides move 16 bytes per access:
+//  1. the CTA reads its 128 x 128-byte source tile with 16-byte loads (eight
+//     threads per 128-byte row segment; narrower loads only when rows are not
+//     16-byte aligned), into shared memory;
+//  2. each thread then assembles whole 16-byte rows of the output blocks (four
+//     4-byte words from rows j, j+32, j+64, j+96 of the tile) and stores them,
+//     so a warp writes 512 contiguous bytes: one whole block.
+// Shared-memory rows are 132 bytes apart, so the 4-byte reads of step 2 (32
+// consecutive rows, one column) fall in 32 different banks.
 #include "prepack.cuh"
 
 namespace nvfp4 {
@@ -23,33 +29,66 @@ struct PrepackBatch {
     int32_t n;
 };
 
-__global__ void __launch_bounds__(256) prepack_scales_kernel(const __grid_constant__ PrepackBatch batch)
+constexpr int kPrepackCols = 128;                    // source columns (bytes) per CTA: 32 blocks
+constexpr int kPrepackStride = kPrepackCols + 4;     // shared-memory row pitch
+constexpr int kPrepackThreads = 256;
+
+__global__ void __launch_bounds__(kPrepackThreads) prepack_scales_kernel(const __grid_constant__ PrepackBatch batch)
 {
-    __shared__ uint8_t tile[128][36];  // 32 bytes per row + 4 padding (keeps rows 4-byte aligned, spreads banks)
-    int j = 0;
-    while (j + 1 < batch.n && (int)blockIdx.x >= batch.job[j + 1].cta_begin)
-        ++j;
-    const PrepackJob &J = batch.job[j];
+    __shared__ __align__(16) uint8_t tile[128 * kPrepackStride];
+    int jn = 0;
+    while (jn + 1 < batch.n && (int)blockIdx.x >= batch.job[jn + 1].cta_begin)
+        ++jn;
+    const PrepackJob &J = batch.job[jn];
     const int local = (int)blockIdx.x - J.cta_begin;
     const int rt = local / J.chunks, ch = local % J.chunks;
-    const int c0 = ch * 32;  // first source column of this CTA (8 blocks x 4 columns)
+    const int c0 = ch * kPrepackCols;                      // first source column of this CTA
+    const int ncols = min(kPrepackCols, J.cols - c0);      // source columns that exist (> 0)
+    const int nblk = min(kPrepackCols / 4, J.col_blocks - ch * (kPrepackCols / 4));  // output blocks
+    const int r0 = rt * 128;
+    const int nrows = min(128, J.rows - r0);
+    const uint8_t *src = J.src + (size_t)r0 * J.cols + c0;
 
-    for (int i = threadIdx.x; i < 128 * 32; i += 256) {
-        const int r = i / 32, c = i % 32;
-        const int gr = rt * 128 + r, gc = c0 + c;
-        tile[r][c] = (gr < J.rows && gc < J.cols) ? J.src[(size_t)gr * J.cols + gc] : (uint8_t)0;
+    // 1. source tile -> shared memory; missing rows and columns read as zero
+    const bool vec16 = ((J.cols & 15) == 0) && ((reinterpret_cast<uintptr_t>(J.src) & 15) == 0);
+    if (vec16) {
+        // ncols is a multiple of 16 here; 8 chunks of 16 bytes per row. All four loads
+        // of a thread are issued before any of them is used.
+        constexpr int kPer = 128 * 8 / kPrepackThreads;
+        uint4 v[kPer];
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = (int)threadIdx.x + k * kPrepackThreads;
+            const int r = i >> 3, q = i & 7;
+            v[k] = make_uint4(0, 0, 0, 0);
+            if (r < nrows && q * 16 < ncols)
+                v[k] = __ldcs(reinterpret_cast<const uint4 *>(src + (size_t)r * J.cols + q * 16));
+        }
+#pragma unroll
+        for (int k = 0; k < kPer; ++k) {
+            const int i = (int)threadIdx.x + k * kPrepackThreads;
+            const int r = i >> 3, q = i & 7;
+            uint32_t *d = reinterpret_cast<uint32_t *>(tile + r * kPrepackStride + q * 16);
+            d[0] = v[k].x, d[1] = v[k].y, d[2] = v[k].z, d[3] = v[k].w;
+        }
+    } else {
+        for (int i = threadIdx.x; i < 128 * kPrepackCols; i += kPrepackThreads) {
+            const int r = i / kPrepackCols, c = i % kPrepackCols;
+            tile[r * kPrepackStride + c] = (r < nrows && c < ncols) ? src[(size_t)r * J.cols + c] : (uint8_t)0;
+        }
     }
     __syncthreads();
 
-    const int cb = threadIdx.x / 32, jj = threadIdx.x % 32;  // block within the chunk, row within the block
-    const int gcb = ch * 8 + cb;
-    if (gcb < J.col_blocks) {
+    // 2. whole 16-byte rows of the output blocks: word (block b, row j) = the four
+    //    columns of block b in rows j, j + 32, j + 64 and j + 96 of the tile
+    uint8_t *dst = J.dst + ((size_t)rt * J.col_blocks + (size_t)ch * (kPrepackCols / 4)) * 512;
+    for (int i = threadIdx.x; i < nblk * 32; i += kPrepackThreads) {
+        const int b = i >> 5, j = i & 31;
         uint32_t w[4];
 #pragma unroll
-        for (int i = 0; i < 4; ++i)
-            w[i] = *reinterpret_cast<const uint32_t *>(&tile[i * 32 + jj][cb * 4]);
-        uint8_t *dst = J.dst + ((size_t)rt * J.col_blocks + gcb) * 512 + jj * 16;
-        *reinterpret_cast<uint4 *>(dst) = make_uint4(w[0], w[1], w[2], w[3]);
+        for (int q = 0; q < 4; ++q)
+            w[q] = *reinterpret_cast<const uint32_t *>(tile + (q * 32 + j) * kPrepackStride + b * 4);
+        __stcs(reinterpret_cast<uint4 *>(dst + (size_t)b * 512 + j * 16), make_uint4(w[0], w[1], w[2], w[3]));
     }
 }
 
@@ -64,14 +103,14 @@ cudaError_t launch_prepack(PrepackJob *jobs, int n, cudaStream_t stream)
             if (J.rows <= 0 || J.cols <= 0)
                 continue;
             J.col_blocks = (J.cols + 3) / 4;
-            J.chunks = (J.col_blocks + 7) / 8;
+            J.chunks = (J.cols + kPrepackCols - 1) / kPrepackCols;
             J.cta_begin = ctas;
             ctas += ((J.rows + 127) / 128) * J.chunks;
             b.job[b.n++] = J;
         }
         if (b.n == 0)
             continue;
-        prepack_scales_kernel<<<ctas, 256, 0, stream>>>(b);
+        prepack_scales_kernel<<<ctas, kPrepackThreads, 0, stream>>>(b);
         cudaError_t e = cudaGetLastError();
         if (e != cudaSuccess)
             return e;

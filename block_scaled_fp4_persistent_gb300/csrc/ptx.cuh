@@ -182,6 +182,17 @@ __device__ __forceinline__ void tensormap_prefetch(const void *tmap)
     asm volatile("prefetch.tensormap [%0];" ::"l"(tmap) : "memory");
 }
 
+// The tensor maps live in global memory, written by the host (cudaMemcpyAsync of
+// the table: generic-proxy writes at system scope), and a later table may reuse the
+// same address. This fence orders those writes before the executing thread's later
+// uses of the 128-byte map at `tmap` through the tensor-map proxy (TMA copies and
+// stores), so a descriptor cached from an earlier launch is never used. Each thread
+// that issues copies through a map runs it before its first use of that map.
+__device__ __forceinline__ void tensormap_acquire(const void *tmap)
+{
+    asm volatile("fence.proxy.tensormap::generic.acquire.sys [%0], 128;" ::"l"(tmap) : "memory");
+}
+
 // 2-D tiled load global -> this CTA's shared memory; completes on `bar`.
 // x is the innermost coordinate (bytes for a uint8 map), y the row.
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const void *tmap, int32_t x, int32_t y, uint32_t bar,

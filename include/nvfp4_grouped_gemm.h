@@ -47,7 +47,8 @@ enum {
     NVFP4_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 (sm_103a) */
     NVFP4_ERR_CUDA = -4,               /* a CUDA runtime or driver call failed; see nvfp4_last_cuda_error() */
     NVFP4_ERR_TIMEOUT = -5,            /* a kernel gave up a bounded wait; reported by nvfp4_device_status() */
-    NVFP4_ERR_TOO_LARGE = -6           /* a size beyond the library's limits (e.g. M, N or K >= 2^24, or 2^23 groups) */
+    NVFP4_ERR_TOO_LARGE = -6,          /* a size beyond the library's limits (e.g. M, N or K >= 2^24, or 2^23 groups) */
+    NVFP4_ERR_CAPTURE = -7             /* nvfp4_grouped_gemm_noalloc called on a stream being captured into a graph */
 };
 
 /* Scale-factor layouts of SFA/SFB. */
@@ -126,6 +127,17 @@ size_t nvfp4_prepacked_scale_bytes(int rows, int K);
  *  K % 16 == 0. Both pointers 16-byte aligned. One launch, stream-ordered.
  *  rows == 0 or K == 0 is a no-op. */
 int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, void *sf_blocked, nvfp4_stream_t stream);
+
+/* The same prepack for n operands at once (e.g. SFA and SFB of every group of a
+ * call): operand i reads sf_rowmajor[i] ([rows[i]][K[i]/16] bytes, device) and
+ * writes sf_blocked[i] (nvfp4_prepacked_scale_bytes(rows[i], K[i]) bytes,
+ * device), with the rules of nvfp4_prepack_scales for each. The four arrays are
+ * host arrays of n entries, read during the call only. One launch for up to 32
+ * operands (more take one launch per 32). Operands with rows == 0 or K == 0 are
+ * skipped; n == 0 is a no-op. Every operand is checked before anything is
+ * launched. */
+int nvfp4_prepack_scales_batch(int n, const void *const *sf_rowmajor, const int *rows, const int *K,
+                               void *const *sf_blocked, nvfp4_stream_t stream);
 
 /* Reads and clears the current device's error word, which kernels set when a
  * bounded wait runs out. Synchronises `stream` first.
@@ -265,14 +277,28 @@ void nvfp4_release(void);
  *    the new table: calls that can overlap on the GPU race and must not be made.
  *  - The first call on each device does a one-time set-up with that device
  *    current: it checks the device, looks up the array's device address
- *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit. Make that
- *    first call before any stream capture.
- *  - The kernel's error words live in the same array. They are cleared at the
- *    start of each call and nvfp4_device_status() does not read them, so a
- *    wait that runs out in this kernel is not reported.
+ *    (cudaGetSymbolAddress) and sets the kernel's shared-memory limit.
+ *  - It must not be captured into a CUDA graph: each call copies its table from
+ *    a static host buffer that the next call overwrites, so a replayed graph
+ *    would launch with another call's table. On a stream that is capturing it
+ *    returns NVFP4_ERR_CAPTURE and queues nothing.
+ *  - The kernel's error words live in the same array and are sticky: a wait that
+ *    runs out records NVFP4_ERR_TIMEOUT there (C may then be partly written).
+ *    nvfp4_noalloc_status() reads and clears them; nvfp4_device_status() does not
+ *    see them.
  * Each call encodes its tensor maps and copies the table (a few KB) from a
  * static host buffer before the launch. There is no cache. */
 int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp4_stream_t stream);
+
+/* The error words of nvfp4_grouped_gemm_noalloc's kernel on the current device,
+ * read and cleared, like nvfp4_device_status() for the other entry point. The
+ * pages have no counterpart. Synchronises `stream` first, then reads the fixed
+ * array through its symbol (cudaMemcpyFromSymbol), so it allocates nothing.
+ *  *status = NVFP4_OK, or NVFP4_ERR_TIMEOUT if a no-allocation launch since the
+ *  last read gave up a wait; detail (may be NULL) receives the 4 words (code,
+ *  role, work item, k-stage), as for nvfp4_device_status().
+ * Returns NVFP4_OK or an NVFP4_ERR_* code of its own. */
+int nvfp4_noalloc_status(nvfp4_stream_t stream, int *status, int32_t *detail);
 
 #ifdef __cplusplus
 }

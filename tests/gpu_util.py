@@ -1,7 +1,12 @@
 """Helpers for the GPU tests: upload generated groups, call the library through the
 C ABI, and check canary guard bands around every output buffer."""
+import functools
+
 import numpy as np
 import torch
+
+import gen
+import oracle
 
 import block_scaled_fp4_persistent_gb300 as nv
 
@@ -52,3 +57,10 @@ def run(dgroups, stream=None):
     torch.cuda.synchronize()
     status, detail = nv.nvfp4_device_status(stream)
     assert status == 0, f"device status {status}: {detail}"
+
+
+@functools.lru_cache(maxsize=None)
+def workload_reference(name):
+    """The oracle's (C, S) for every output of a named workload, computed once per test
+    session (the full-size sets take the oracle about a second or two on the host's cores)."""
+    return oracle.grouped_gemm(gen.make_workload(name))

@@ -5,9 +5,8 @@ Bars:
  * GEMM: every compared output within |C_gpu - C_oracle| <= 1e-3 * S + 1 ulp16;
  * no store outside C (4 KB canary bands on both sides) and no output left unwritten;
  * results independent of the pipeline depth and of the number of CTAs, bit for bit.
-Small workloads compare every output. The full-size workloads run in the launch
-configuration the benchmark uses and compare sampled outputs, computed one by
-one by the oracle.
+Every test compares every output, the full-size workloads included (in the launch
+configuration the benchmark uses, and in the others).
 """
 import numpy as np
 import pytest
@@ -17,7 +16,7 @@ import gen
 import oracle
 from parity import assert_within_bound
 import block_scaled_fp4_persistent_gb300 as nv
-from gpu_util import DeviceGroup, run
+from gpu_util import DeviceGroup, run, workload_reference
 
 pytestmark = pytest.mark.gpu
 
@@ -314,34 +313,25 @@ def test_two_streams_at_once_with_split_tails():
         check_full(groups, d, "two streams")
 
 
-# --------------------------------------------------------- full-size, sampled ---
-
-def sample_indices(M, N, n, rng):
-    ms = list(rng.integers(0, M, n)) + [0, M - 1, 0, M - 1] + [M - 1] * 8 + list(range(min(M, 8)))
-    ns = list(rng.integers(0, N, n)) + [0, 0, N - 1, N - 1] + list(rng.integers(0, N, 8)) + [N - 1] * min(M, 8)
-    return np.array(ms), np.array(ns)
-
+# ------------------------------------------------------- full-size, every output ---
 
 @pytest.mark.parametrize("pair,layout", [(0, nv.NVFP4_SF_PREPACKED), (1, nv.NVFP4_SF_ROWMAJOR),
                                          (2, nv.NVFP4_SF_PREPACKED), (2, nv.NVFP4_SF_ROWMAJOR)])
 @pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
-def test_full_size_workloads_sampled(name, pair, layout):
+def test_full_size_workloads_every_output(name, pair, layout):
     # pair 0: the automatic choice with prepacked scales, the benchmark's launch
     # configuration; 1: CTA pairs; 2: single CTAs (which split the MoE sets' last
     # wave along K). Row-major scales are read in the kernel (the e2e benchmark's route).
+    # Every output is compared with the oracle's.
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_workload(name)
     d = [DeviceGroup(g, layout) for g in groups]
     run(d)  # default options: the launch configuration of the benchmark
-    rng = np.random.default_rng(99)
-    again = None
-    for i, (g, x) in enumerate(zip(groups, d)):
+    for i, (x, (c_ref, s_ref)) in enumerate(zip(d, workload_reference(name))):
         got = x.result()
         assert not np.isnan(got).any(), f"{name} group {i}: unwritten outputs"
         assert x.guards_intact()
-        ms, ns = sample_indices(g.M, g.N, 3000, rng)
-        c_ref, s_ref = oracle.gemm_entries(g, ms, ns)
-        assert_within_bound(got[ms, ns], c_ref, s_ref, f"{name} group {i}")
+        assert_within_bound(got, c_ref, s_ref, f"{name} group {i}")
     # a property that holds at any size: a second launch gives the same bits
     first = [x.result().copy() for x in d]
     for x in d:
