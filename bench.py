@@ -68,6 +68,7 @@ NOMINAL_FP4_TFLOPS = 13500.0  # dense NVFP4, GB300
 # number, reported as context through vs_baseline, not a target.
 PAGES_BEST_US = {"moe_g8_n4096_k7168": 47.5, "moe_g8_n7168_k2048": 45.0, "g2_n3072_k4096": 14.3,
                  "g2_n4096_k1536": 10.5}
+KERNEL_CHOICE = {"auto": 0, "pair": 1, "single": 2, "swapab": 3, "swapab_pair": 4}  # values of NVFP4_OPT_CTA_PAIR
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
 KERNEL_SOURCES = ["block_scaled_fp4_persistent_gb300/csrc/gemm_kernel.cuh",
                   "block_scaled_fp4_persistent_gb300/csrc/pair_kernel.cuh",
@@ -605,6 +606,7 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
         "data": "synthetic (SplitMix64 seeded generator; shapes and distributions of the leaderboard workload)",
         "config": {"workload": args.workload, "g": len(groups), "M": [g.M for g in groups],
                    "N": [g.N for g in groups], "K": [g.K for g in groups], "seed": gen.WORKLOADS[args.workload]["seed"],
+                   "kernel_choice": args.kernel,
                    "scales": "prepacked 128x4 blocked layout", "l2": "flushed before every timed call "
                    "(2xL2 write, then 2xL2 read)", "parallelism": f"replicas x{world}"},
         "median_us": round(med_us, 3),
@@ -693,6 +695,8 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="moe_g8_n4096_k7168", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_CHOICE),
+                    help="kernel kind (NVFP4_OPT_CTA_PAIR): the library's automatic choice by default")
     ap.add_argument("--e2e-steps", type=int, default=100)
     ap.add_argument("--cpu-seconds", type=float, default=15.0, help="budget of the oracle timing sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -747,6 +751,9 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl", device_id=torch.device("cuda", local_rank))
+    if args.kernel != "auto":
+        import block_scaled_fp4_persistent_gb300 as nv
+        nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, KERNEL_CHOICE[args.kernel])
     # each rank draws its own replica of the workload (weak scaling)
     groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
     out = run_ours(args, groups, rank, world, local_rank)

@@ -175,6 +175,33 @@ __device__ __forceinline__ void prefetch_scale_maps(const Table *tab, int num_gr
     }
 }
 
+// The A and B maps of group g: from the launch parameters for the first
+// kParamMapGroups groups, else from the table (those take an acquire fence before a
+// thread's first use, see acquire_table_maps).
+__device__ __forceinline__ const CUtensorMap *map_a(const KernelArgs &args, const Table *tab, int g)
+{
+    return g < kParamMapGroups ? &args.pmaps[2 * g] : &tab->group(g).tmap_a;
+}
+__device__ __forceinline__ const CUtensorMap *map_b(const KernelArgs &args, const Table *tab, int g)
+{
+    return g < kParamMapGroups ? &args.pmaps[2 * g + 1] : &tab->group(g).tmap_b;
+}
+
+// The C map of group g (the epilogues' stores), by the same rule.
+__device__ __forceinline__ const CUtensorMap *map_c(const KernelArgs &args, const Table *tab, int g)
+{
+    return g < kParamMapGroups ? &args.cmaps[g] : &tab->group(g).tmap_c;
+}
+
+// Prefetch of the table's A and B maps of groups kParamMapGroups .. 63, by a warp's lanes.
+__device__ __forceinline__ void prefetch_table_maps(const Table *tab, int num_groups, uint32_t lane)
+{
+    for (int i = 2 * kParamMapGroups + (int)lane; i < 2 * min(num_groups, 64); i += 32) {
+        const GroupEntry &g = tab->group(i / 2);
+        tensormap_prefetch(i % 2 == 0 ? &g.tmap_a : &g.tmap_b);
+    }
+}
+
 __device__ __forceinline__ WorkItem global_item(const KernelArgs &args, uint32_t it)
 {
     const int4 *p = args.items + 4 * (size_t)it;
@@ -328,13 +355,10 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
         first_item = global_item(args, item_begin);
-    // The groups' operand tensor maps, fetched ahead by the producer warp's lanes
-    // in parallel: one prefetch.tensormap per lane.
+    // The operand maps of groups past those in the launch parameters, fetched ahead by
+    // the producer warp's lanes in parallel.
     if (warp == kProducerWarp)
-        for (int i = (int)lane; i < 2 * min(args.num_groups, 64); i += 32) {
-            const GroupEntry &g = tab->group(i / 2);
-            tensormap_prefetch(i % 2 == 0 ? &g.tmap_a : &g.tmap_b);
-        }
+        prefetch_table_maps(tab, args.num_groups, lane);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -396,8 +420,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                 const WorkItem w = it == item_begin ? first_item : global_item(args, it);
                 const GroupEntry &ge = tab->group(w.group);  // address only: no load
                 r.group = w.group;
-                r.tmap_a = &ge.tmap_a;  // one A map per group: M-fusion is for CTA pairs only
-                r.tmap_b = &ge.tmap_b;
+                r.tmap_a = map_a(args, tab, w.group);  // one A map per group: M-fusion is for CTA pairs only
+                r.tmap_b = map_b(args, tab, w.group);
                 r.ya = w.tile_m * kBlockM;
                 r.yb = w.tile_n * BN;
                 r.kb64 = w.kblocks64;
@@ -416,16 +440,18 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                     r.sfb[L::kHalves - 1] = w.sfb + ((w.flags & kItemB2) ? (size_t)r.kb64 * kScaleBlockBytes : 0);
                 return r;
             };
-            // Before this thread's first copy (or prefetch) through a group's maps, the
-            // acquire fence for each of them (see tensormap_acquire). Items come group by
-            // group, so this runs about once per group.
+            // Maps read from the table (A and B of groups past the launch parameters, and
+            // the row-major scale maps) get their acquire fence here, before this thread's
+            // first copy (or prefetch) through them.
             int fenced = -1;
             auto acquire_maps = [&](const Src &s) {
                 if (s.group == fenced)
                     return;
                 fenced = s.group;
-                tensormap_acquire(s.tmap_a);
-                tensormap_acquire(s.tmap_b);
+                if (s.group >= kParamMapGroups) {
+                    tensormap_acquire(s.tmap_a);
+                    tensormap_acquire(s.tmap_b);
+                }
                 if (s.sf_rowmajor) {
                     tensormap_acquire(s.tmap_sfa);
                     tensormap_acquire(s.tmap_sfb);
@@ -628,14 +654,15 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
-        int fenced = -1;  // the group whose C map lane 0 last fenced (it issues the stores)
+        int fenced = -1;  // the group whose C map lane 0 (which issues the stores) last fenced
         grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
-            if (lane == 0 && w.group != fenced) {
-                tensormap_acquire(&ge.tmap_c);
+            // before the wait for the accumulator, so that the fence overlaps the MMAs
+            if (lane == 0 && w.group >= kParamMapGroups && w.group != fenced) {
+                tensormap_acquire(map_c(args, tab, w.group));
                 fenced = w.group;
             }
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
@@ -668,7 +695,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
 #pragma unroll
                     for (int c = 0; c < kCols / 32; ++c)
                         if (n0 + c * 32 < N)
-                            out.store(&ge.tmap_c, n0 + c * 32, m_row0, h[c], lane);
+                            out.store(map_c(args, tab, w.group), n0 + c * 32, m_row0, h[c], lane);
                 }
             } else {
                 // One segment of a split tile: its fp32 partial goes to the workspace slot.
@@ -747,7 +774,7 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
                                     h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
                                     h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
                                 }
-                                out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
+                                out.store(map_c(args, tab, w.group), n0 + c * 32, m_row0, h, lane);
                             }
                         }
                     }

@@ -30,6 +30,8 @@
 #include "gemm_kernel.cuh"
 #include "pair_kernel.cuh"
 #include "prepack.cuh"
+#include "swapab_kernel.cuh"
+#include "swapab_pair_kernel.cuh"
 #include "table.h"
 
 using namespace nvfp4;
@@ -91,7 +93,13 @@ constexpr int kDefaultStages = kDefaultBlockN == 256 ? kDeepStages256 : kDeepSta
 // The CTA-pair kernel: 256 x 256 tiles, 5 x 38 KB ring (its TMEM holds 5 scale slots).
 constexpr int kPairStages = 5;
 constexpr int kVariantPair = 4;
-constexpr int kVariantAuto = -1;  // chosen per problem set: CTA pairs or single CTAs with 128 x 128 tiles
+// The swapped-operand kernel (swap-AB): 128 rows of B on the MMA's M side, a group's
+// rows of A (up to 2 x 128 per item) on its N side, stream-K over all SMs.
+constexpr int kVariantSwap = 5;
+// The same on CTA pairs: 256 rows of B on the MMA's M side (128 per SM), up to 256 rows
+// of A on its N side (half per SM), stream-K over the pairs.
+constexpr int kVariantSwapPair = 6;
+constexpr int kVariantAuto = -1;  // chosen per problem set
 // How far ahead of the ring the producer prefetches into L2, in stages.
 constexpr int kDefaultPrefetchStages = 0;
 constexpr int kMaxDim = 1 << 24;
@@ -430,6 +438,24 @@ int encode_output_map(CUtensorMap *map, void *C, uint64_t M, uint64_t N)
     return NVFP4_OK;
 }
 
+// The fp16 output [M][N] as boxes of 16 rows x 32 columns, unswizzled: the swapped
+// kernel's transposed epilogue stores one such box per 16 rows of A and 32 of B.
+int encode_output_map_t(CUtensorMap *map, void *C, uint64_t M, uint64_t N)
+{
+    cuuint64_t dims[2] = {N, M};
+    cuuint64_t strides[1] = {N * 2};
+    cuuint32_t box[2] = {32, 16};
+    cuuint32_t estr[2] = {1, 1};
+    CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, C, dims, strides, box, estr,
+                          CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_NONE,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    if (r != CUDA_SUCCESS) {
+        g_last_cuda_error.store(10000 + (int)r);
+        return NVFP4_ERR_CUDA;
+    }
+    return NVFP4_OK;
+}
+
 int check_problem(const Nvfp4Problem &p)
 {
     if (p.M < 0 || p.N < 0 || p.K < 0)
@@ -597,6 +623,234 @@ Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int blo
     return sc;
 }
 
+// ------------------------------------------------------ swap-AB schedule --
+//
+// Tiles of the swapped-operand kernel, numbered group by group, then by 128-row
+// tile w of B, then by item p: item p of tile w covers the 128-row tiles 2p and
+// 2p + 1 of A (one where the group has an odd number). An item's cost is its
+// shared-memory stages: K-stages x token tiles. With stream-K the items are laid
+// end to end and cut into grid-many equal spans at K-stage boundaries; a cut that
+// would leave fewer than kSwapMinSeg K-stages on either side of a tile moves to
+// the tile's edge. A tile cut into several segments is a split tile (fp32
+// partials, summed in K order by the last segment to finish). Without stream-K
+// (or where it would not shorten the busiest CTA) whole items go to the CTAs
+// longest first, each to the least loaded.
+constexpr int kSwapMinSeg = 2;
+
+struct SwapTile {
+    int group, w, t0, ntok, nk;
+};
+
+inline int round16(int x) { return (x + 15) / 16 * 16; }
+
+WorkItem make_swap_item(const ActiveGroup &g, int gi, const SwapTile &t, int kb_begin, int kb_end, int split, int seg,
+                        int nseg, int slot)
+{
+    WorkItem w{};
+    w.group = gi;
+    w.tile_m = t.t0;
+    w.tile_n = t.w;
+    w.kb_begin = kb_begin;
+    w.kb_end = kb_end;
+    w.split = split;
+    w.seg = seg;
+    w.nseg = nseg;
+    w.ws_slot = slot;
+    const int kb64 = g.K / 64;
+    w.kblocks64 = kb64;
+    const int ntt = (g.M + kSwapTileRows - 1) / kSwapTileRows;
+    const int nt0 = round16(std::min(kSwapTileRows, g.M - kSwapTileRows * t.t0));
+    const int nt1 = t.ntok == 2 ? round16(std::min(kSwapTileRows, g.M - kSwapTileRows * (t.t0 + 1))) : 0;
+    const int box = g.M <= kSwapTileRows ? round16(g.M) : kSwapTileRows;
+    w.flags = ((ntt + 1) / 2 > 1 ? kItemBShared : 0) | (g.sf_rowmajor ? kItemSfRowMajor : 0) |
+              ((nt0 / 16) << kSwapNt0Shift) | ((nt1 / 16) << kSwapNt1Shift) | ((box / 16) << kSwapBoxShift);
+    w.a_row = kSwapTileRows * t.t0;
+    const size_t blocks = (size_t)kb64 * kScaleBlockBytes;
+    w.sfa = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFA) + (size_t)t.t0 * blocks);
+    w.sfb = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFB) + (size_t)t.w * blocks);
+    return w;
+}
+
+// Lists for grid_cap CTAs (or CTA pairs) over `tiles` in their order, each tile
+// costing nk * ntok stages: whole tiles longest first, each to the least loaded list,
+// or stream-K spans (see above), whichever leaves the busiest list shorter (a split
+// segment counted two stages dearer). make(tile, kb_begin, kb_end, split, seg, nseg,
+// slot) builds an item; a split tile takes `ntok` split ids and each of its segments
+// `ntok` slots. Lists that come out empty are dropped.
+template <class Make>
+Schedule stream_k_schedule(const std::vector<SwapTile> &tiles, int grid_cap, bool stream_k, Make make)
+{
+    Schedule sc;
+    const size_t T = tiles.size();
+    std::vector<int64_t> start(T + 1, 0);
+    for (size_t t = 0; t < T; ++t)
+        start[t + 1] = start[t] + (int64_t)tiles[t].nk * tiles[t].ntok;
+    const int64_t U = start[T];
+
+    // whole items, longest first, each to the least loaded CTA
+    const int Gw = std::max(1, std::min<int>((int)T, grid_cap));
+    std::vector<int> owner(T, 0);
+    std::vector<int64_t> load(Gw, 0);
+    {
+        std::vector<size_t> order(T);
+        for (size_t t = 0; t < T; ++t)
+            order[t] = t;
+        std::stable_sort(order.begin(), order.end(), [&](size_t a, size_t b) {
+            return start[a + 1] - start[a] > start[b + 1] - start[b];
+        });
+        for (size_t t : order) {
+            int best = 0;
+            for (int c = 1; c < Gw; ++c)
+                if (load[c] < load[best])
+                    best = c;
+            owner[t] = best;
+            load[best] += start[t + 1] - start[t];
+        }
+    }
+    const int64_t makespan_whole = *std::max_element(load.begin(), load.end());
+
+    // stream-K spans
+    const int Gs = std::max(1, grid_cap);
+    std::vector<int64_t> b(Gs + 1, 0);
+    b[Gs] = U;
+    for (int c = 1; c < Gs; ++c) {
+        const int64_t x = ((int64_t)c * U + Gs / 2) / Gs;
+        const size_t t = (size_t)(std::upper_bound(start.begin(), start.end(), x) - start.begin()) - 1;
+        int64_t snapped = x;
+        if (t < T) {
+            const int ntok = tiles[t].ntok, nk = tiles[t].nk;
+            int kb = (int)((x - start[t] + ntok / 2) / ntok);
+            if (kb < kSwapMinSeg)
+                kb = 0;
+            else if (nk - kb < kSwapMinSeg)
+                kb = nk;
+            snapped = start[t] + (int64_t)kb * ntok;
+            // nor a short segment after the previous cut inside the same tile
+            if (b[c - 1] > start[t] && snapped > b[c - 1] && snapped - b[c - 1] < (int64_t)kSwapMinSeg * ntok)
+                snapped = b[c - 1];
+        }
+        b[c] = std::max(snapped, b[c - 1]);
+    }
+    int64_t makespan_sk = 0;
+    for (int c = 0; c < Gs; ++c) {
+        int64_t cost = b[c + 1] - b[c];
+        const size_t t_lo = (size_t)(std::upper_bound(start.begin(), start.end(), b[c]) - start.begin()) - 1;
+        if (b[c + 1] > b[c] && t_lo < T && b[c] > start[t_lo])
+            cost += 2;
+        const size_t t_hi = (size_t)(std::upper_bound(start.begin(), start.end(), b[c + 1] - 1) - start.begin()) - 1;
+        if (b[c + 1] > b[c] && t_hi < T && b[c + 1] < start[t_hi + 1])
+            cost += 2;
+        makespan_sk = std::max(makespan_sk, cost);
+    }
+    const bool use_sk = stream_k && T > 0 && makespan_sk < makespan_whole;
+
+    const int G = use_sk ? Gs : Gw;
+    std::vector<std::vector<WorkItem>> per(G);
+    if (!use_sk) {
+        for (size_t t = 0; t < T; ++t)
+            per[owner[t]].push_back(make(tiles[t], 0, tiles[t].nk, -1, 0, 1, 0));
+    } else {
+        int c = 0;
+        for (size_t t = 0; t < T; ++t) {
+            const SwapTile &x = tiles[t];
+            const int64_t s0 = start[t], s1 = start[t + 1];
+            while (c < G && b[c + 1] <= s0)
+                ++c;
+            std::vector<std::pair<int, std::pair<int, int>>> segs;
+            for (int cc = c; cc < G && b[cc] < s1; ++cc) {
+                const int64_t lo = std::max(s0, b[cc]), hi = std::min(s1, b[cc + 1]);
+                if (hi > lo)
+                    segs.push_back({cc, {(int)((lo - s0) / x.ntok), (int)((hi - s0) / x.ntok)}});
+            }
+            const int nseg = (int)segs.size();
+            const int split = nseg > 1 ? sc.splits : -1;
+            if (nseg > 1)
+                sc.splits += x.ntok;
+            for (int j = 0; j < nseg; ++j) {
+                const int slot = nseg > 1 ? sc.ws_slots : 0;
+                if (nseg > 1)
+                    sc.ws_slots += x.ntok;
+                per[segs[j].first].push_back(make(x, segs[j].second.first, segs[j].second.second, split, j, nseg, slot));
+            }
+        }
+    }
+    // CTAs whose span came out empty (cuts moved to tile edges) are not launched
+    per.erase(std::remove_if(per.begin(), per.end(), [](const std::vector<WorkItem> &l) { return l.empty(); }),
+              per.end());
+    if (per.empty())
+        per.resize(1);
+    sc.grid = (int)per.size();
+    sc.list_begin.assign(sc.grid + 1, 0);
+    for (int l = 0; l < sc.grid; ++l) {
+        sc.list_begin[l] = (uint32_t)sc.items.size();
+        sc.items.insert(sc.items.end(), per[l].begin(), per[l].end());
+    }
+    sc.list_begin[sc.grid] = (uint32_t)sc.items.size();
+    return sc;
+}
+
+Schedule build_swap_schedule(const std::vector<ActiveGroup> &gs, int grid_cap, bool stream_k)
+{
+    std::vector<SwapTile> tiles;
+    for (int gi = 0; gi < (int)gs.size(); ++gi) {
+        const ActiveGroup &g = gs[gi];
+        const int ntt = (g.M + kSwapTileRows - 1) / kSwapTileRows, tw = (g.N + kSwapTileRows - 1) / kSwapTileRows;
+        const int nk = (g.K / 64 + 3) / 4;
+        for (int w = 0; w < tw; ++w)
+            for (int t0 = 0; t0 < ntt; t0 += 2)
+                tiles.push_back(SwapTile{gi, w, t0, std::min(2, ntt - t0), nk});
+    }
+    return stream_k_schedule(tiles, grid_cap, stream_k,
+                             [&](const SwapTile &t, int kb0, int kb1, int split, int seg, int nseg, int slot) {
+                                 return make_swap_item(gs[t.group], t.group, t, kb0, kb1, split, seg, nseg, slot);
+                             });
+}
+
+// The pair kernel's item: B rows 256w .. 256w + 255 (tile_n = w), A rows 256t .. (tile_m
+// = t), the group's MMA width in the flags. The scale blocks of the first 128-row tiles
+// of both; the second ones follow (kItemA2 / kItemB2 say whether they exist).
+WorkItem make_swap_pair_item(const ActiveGroup &g, int gi, const SwapTile &t, int kb_begin, int kb_end, int split,
+                             int seg, int nseg, int slot)
+{
+    WorkItem w{};
+    w.group = gi;
+    w.tile_m = t.t0;
+    w.tile_n = t.w;
+    w.kb_begin = kb_begin;
+    w.kb_end = kb_end;
+    w.split = split;
+    w.seg = seg;
+    w.nseg = nseg;
+    w.ws_slot = slot;
+    const int kb64 = g.K / 64;
+    w.kblocks64 = kb64;
+    const int nt = round16(std::min(g.M, kSwapPairRows));
+    w.flags = (kSwapPairRows * t.w + 128 < g.N ? kItemA2 : 0) | (kSwapPairRows * t.t0 + 128 < g.M ? kItemB2 : 0) |
+              (g.sf_rowmajor ? kItemSfRowMajor : 0) | ((nt / 16) << kSwapPairNtShift);
+    w.a_row = kSwapPairRows * t.t0;
+    const size_t blocks = (size_t)kb64 * kScaleBlockBytes;
+    w.sfa = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFA) + (size_t)(2 * t.t0) * blocks);
+    w.sfb = reinterpret_cast<const uint8_t *>(reinterpret_cast<uintptr_t>(g.SFB) + (size_t)(2 * t.w) * blocks);
+    return w;
+}
+
+Schedule build_swap_pair_schedule(const std::vector<ActiveGroup> &gs, int grid_cap, bool stream_k)
+{
+    std::vector<SwapTile> tiles;
+    for (int gi = 0; gi < (int)gs.size(); ++gi) {
+        const ActiveGroup &g = gs[gi];
+        const int ntt = (g.M + kSwapPairRows - 1) / kSwapPairRows, tw = (g.N + kSwapPairRows - 1) / kSwapPairRows;
+        const int nk = (g.K / 64 + 3) / 4;
+        for (int w = 0; w < tw; ++w)
+            for (int t = 0; t < ntt; ++t)
+                tiles.push_back(SwapTile{gi, w, t, 1, nk});
+    }
+    return stream_k_schedule(tiles, grid_cap, stream_k,
+                             [&](const SwapTile &t, int kb0, int kb1, int split, int seg, int nseg, int slot) {
+                                 return make_swap_pair_item(gs[t.group], t.group, t, kb0, kb1, split, seg, nseg, slot);
+                             });
+}
+
 // How one kernel variant tiles a problem set.
 struct Plan {
     int variant;
@@ -606,11 +860,11 @@ struct Plan {
 
 Plan plan_for(int variant, const DeviceState &ds, int64_t max_ctas)
 {
-    const bool pair = variant == kVariantPair;
+    const bool pair = variant == kVariantPair || variant == kVariantSwapPair;
     Plan p;
     p.variant = variant;
     p.block_m = pair ? kPairBlockM : kBlockM;
-    p.block_n = pair ? kPairBlockN : (variant >= 2 ? 256 : 128);
+    p.block_n = pair ? kPairBlockN : ((variant == 2 || variant == 3) ? 256 : 128);
     int cap = std::min(pair ? ds.pair_clusters : ds.sm_count, kMaxLists);
     if (max_ctas > 0)
         cap = (int)std::min<int64_t>(pair ? std::max<int64_t>(1, max_ctas / 2) : max_ctas, cap);
@@ -652,6 +906,16 @@ double makespan_us(const Schedule &sc, double stage_us)
 // stay on single CTAs (16.6 against about 18; 12.3 against about 14).
 int choose_variant(const std::vector<ActiveGroup> &gs, const DeviceState &ds, int64_t max_ctas, int split_mode)
 {
+    // Every group with at most 32 rows of A (decode-sized MoE sets): the swapped-operand
+    // kernel, whose MMA is only as wide as the rows there are. Measured on this GPU,
+    // against the best of the others: M 1-8, N 7168, K 2048: 20.6 against 22.0 us;
+    // M 4-32, N 4096, K 7168: 33.5 against 35.0; 32 groups of M 8, N 4096, K 7168: 104
+    // against 109. With 48-96 rows per group the unswapped kernels are ahead again.
+    int max_m = 0;
+    for (const ActiveGroup &g : gs)
+        max_m = std::max(max_m, g.M);
+    if (max_m <= 32)
+        return kVariantSwap;
     const Plan pp = plan_for(kVariantPair, ds, max_ctas), p1 = plan_for(0, ds, max_ctas);
     const double t_pair = 1.0 + makespan_us(build_schedule(gs, pp.block_m, pp.block_n, pp.grid_cap,
                                                            split_for(kVariantPair, split_mode)),
@@ -736,18 +1000,24 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     // The pair kernel (variant kVariantPair) runs 256 x 256 tiles, one list per CTA pair.
     const int variant = variant_req == kVariantAuto ? choose_variant(gs, ds, max_ctas, split_mode) : variant_req;
     const Plan plan = plan_for(variant, ds, max_ctas);
-    const bool pair = variant == kVariantPair;
+    const bool swap_pair = variant == kVariantSwapPair;
+    const bool pair = variant == kVariantPair || swap_pair;
+    const bool swap = variant == kVariantSwap || swap_pair;
     const int block_m = plan.block_m, block_n = plan.block_n;
     const int halves = pair ? 2 : 1;  // workspace slots and counters per split segment / tile
-    Schedule sc = build_schedule(gs, block_m, block_n, plan.grid_cap, split_for(variant, split_mode));
+    Schedule sc = swap_pair ? build_swap_pair_schedule(gs, plan.grid_cap, split_mode != 0)
+                  : swap    ? build_swap_schedule(gs, plan.grid_cap, split_mode != 0)
+                            : build_schedule(gs, block_m, block_n, plan.grid_cap, split_for(variant, split_mode));
     // M-fusion for the pair kernel only: the single-CTA kernel addressing A through
     // the item's row rather than its tile index measured ~1 us slower on the small
-    // two-group sets it serves (which have no runs to fuse anyway).
-    const ARuns runs = a_runs(gs, m_fusion != 0 && pair);
-    for (WorkItem &w : sc.items) {
-        w.a_row += runs.row0[w.group];
-        w.flags = (w.flags & ((1 << kItemAMapShift) - 1)) | (runs.head[w.group] << kItemAMapShift);
-    }
+    // two-group sets it serves (which have no runs to fuse anyway). The swapped
+    // kernel's item flags carry its MMA shapes instead of an A map.
+    const ARuns runs = a_runs(gs, m_fusion != 0 && pair && !swap);
+    if (!swap)
+        for (WorkItem &w : sc.items) {
+            w.a_row += runs.row0[w.group];
+            w.flags = (w.flags & ((1 << kItemAMapShift) - 1)) | (runs.head[w.group] << kItemAMapShift);
+        }
     const std::vector<WorkItem> &items = sc.items;
     const std::vector<uint32_t> &cta_begin = sc.list_begin;
     const int grid = sc.grid;  // lists: CTAs, or CTA pairs
@@ -794,25 +1064,32 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         // A run's later groups keep a copy of its map, so every group's maps stay
         // valid descriptors; the items read the first group's.
         int rc = 0;
+        // the swapped kernels' A box: the group's rows (rounded up to 16) when they fit one
+        // tile; on CTA pairs each CTA holds half of them
+        const uint32_t a_box = swap_pair ? (uint32_t)(round16(std::min(a.M, kSwapPairRows)) / 2)
+                               : swap    ? (uint32_t)(a.M <= kSwapTileRows ? round16(a.M) : kSwapTileRows)
+                                         : (uint32_t)kBlockM;
         if (h == (int)i)
-            rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, run_rows, kBlockM);
+            rc = encode_operand_map(&e.tmap_a, a.A, (uint64_t)a.K / 2, run_rows, a_box);
         else
             e.tmap_a = ge[h].tmap_a;
         if (!rc)
             rc = encode_operand_map(&e.tmap_b, a.B, (uint64_t)a.K / 2, (uint64_t)a.N, pair ? 128u : (uint32_t)block_n);
         if (!rc)
-            rc = encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
+            rc = swap ? encode_output_map_t(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N)
+                      : encode_output_map(&e.tmap_c, a.C, (uint64_t)a.M, (uint64_t)a.N);
         if (!rc) {
             if (!a.sf_rowmajor)
                 rc = encode_unused_scale_map(&e.tmap_sfa, a.SFA);
             else if (h == (int)i)
-                rc = encode_scale_map(&e.tmap_sfa, a.SFA, (uint64_t)a.K / 16, run_rows, kBlockM);
+                rc = encode_scale_map(&e.tmap_sfa, a.SFA, (uint64_t)a.K / 16, run_rows,
+                                      swap_pair ? (uint32_t)kSwapPairRows : (uint32_t)kBlockM);
             else
                 e.tmap_sfa = ge[h].tmap_sfa;
         }
         if (!rc)
             rc = a.sf_rowmajor ? encode_scale_map(&e.tmap_sfb, a.SFB, (uint64_t)a.K / 16, (uint64_t)a.N,
-                                                  pair ? (uint32_t)kPairBlockN : (uint32_t)block_n)
+                                                  swap ? 128u : pair ? (uint32_t)kPairBlockN : (uint32_t)block_n)
                                : encode_unused_scale_map(&e.tmap_sfb, a.SFB);
         if (rc) {
             return_buffers(std::move(t.buf), false);
@@ -863,6 +1140,19 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     return note_use(g_tables.front(), stream);
 }
 
+// The A, B and C maps of the first kParamMapGroups groups, copied from the table's
+// host copy into the launch parameters.
+void fill_param_maps(KernelArgs &args, const void *host_table, int num_groups)
+{
+    const GroupEntry *ge = reinterpret_cast<const GroupEntry *>(static_cast<const uint8_t *>(host_table) +
+                                                                sizeof(TableHeader));
+    for (int g = 0; g < std::min(num_groups, kParamMapGroups); ++g) {
+        args.pmaps[2 * g] = ge[g].tmap_a;
+        args.pmaps[2 * g + 1] = ge[g].tmap_b;
+        args.cmaps[g] = ge[g].tmap_c;
+    }
+}
+
 // Sets the kernel's shared-memory limit once per device and checks that one CTA
 // fits on an SM.
 template <int BN, int STAGES>
@@ -898,6 +1188,7 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
                                                                        : g_opt.prefetch_stages.load());
     args.workspace = t.workspace;
     args.counters = t.counters;
+    fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<BN, STAGES>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     static_assert(kDeepStages128 == 5 && kDeepStages256 == 3, "kernel names below");
@@ -943,9 +1234,82 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.prefetch_stages = 0;
     args.workspace = t.workspace;
     args.counters = t.counters;
+    fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
     CUDA_TRY(launch_kernel(nvfp4_pair_gemm_kernel<kPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_pair_gemm_kernel<5>");
+    return NVFP4_OK;
+}
+
+int prepare_swap_kernel(DeviceState &ds)
+{
+    using L = SwapLayout<kSwapStages>;
+    auto kern = nvfp4_swapab_gemm_kernel<kSwapStages>;
+    if (L::kSmemBytes > ds.max_smem_optin)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (!ds.attr_set[kVariantSwap]) {
+        CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes));
+        int n = 0;
+        CUDA_TRY(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kern, kThreads, L::kSmemBytes));
+        if (n < 1)
+            return NVFP4_ERR_UNSUPPORTED_DEVICE;
+        ds.attr_set[kVariantSwap] = true;
+    }
+    return NVFP4_OK;
+}
+
+int launch_swap(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
+{
+    using L = SwapLayout<kSwapStages>;
+    KernelArgs args{};
+    args.table = static_cast<const Table *>(t.dev);
+    args.items = table_items(t);
+    args.status = ds.status;
+    args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
+    args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
+    args.num_groups = num_groups;
+    args.prefetch_stages = 0;
+    args.workspace = t.workspace;
+    args.counters = t.counters;
+    fill_param_maps(args, t.host, num_groups);
+    std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
+    CUDA_TRY(launch_kernel(nvfp4_swapab_gemm_kernel<kSwapStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
+    static_assert(kSwapStages == 5, "kernel name below");
+    g_last_kernel.store("nvfp4_swapab_gemm_kernel<5>");
+    return NVFP4_OK;
+}
+
+int prepare_swap_pair_kernel(DeviceState &ds)
+{
+    using L = SwapPairLayout<kSwapPairStages>;
+    auto kern = nvfp4_swapab_pair_kernel<kSwapPairStages>;
+    if (L::kSmemBytes > ds.max_smem_optin)
+        return NVFP4_ERR_UNSUPPORTED_DEVICE;
+    if (!ds.attr_set[kVariantSwapPair]) {
+        CUDA_TRY(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, L::kSmemBytes));
+        ds.attr_set[kVariantSwapPair] = true;
+    }
+    return NVFP4_OK;
+}
+
+int launch_swap_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
+{
+    using L = SwapPairLayout<kSwapPairStages>;
+    KernelArgs args{};
+    args.table = static_cast<const Table *>(t.dev);
+    args.items = table_items(t);
+    args.status = ds.status;
+    args.timeout_ns = (uint64_t)std::max<int64_t>(1, g_opt.timeout_us.load()) * 1000ull;
+    args.fault_skip_load = (int32_t)g_opt.fault_skip_load.load();
+    args.num_groups = num_groups;
+    args.prefetch_stages = 0;
+    args.workspace = t.workspace;
+    args.counters = t.counters;
+    fill_param_maps(args, t.host, num_groups);
+    std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
+    CUDA_TRY(launch_kernel(nvfp4_swapab_pair_kernel<kSwapPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
+    static_assert(kSwapPairStages == 5, "kernel name below");
+    g_last_kernel.store("nvfp4_swapab_pair_kernel<5>");
     return NVFP4_OK;
 }
 
@@ -1051,9 +1415,11 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     const int64_t opt_pair = g_opt.cta_pair.load();
     const int single = (block_n == 256 ? 2 : 0) + (shallow ? 1 : 0);
     const int variant_req = opt_pair == 1 ? kVariantPair
+                            : opt_pair == 3 ? kVariantSwap
+                            : opt_pair == 4 ? kVariantSwapPair
                             : (opt_pair == 2 || opt_bn != 0 || shallow) ? single
                                                                         : kVariantAuto;
-    if (variant_req == kVariantPair || variant_req == kVariantAuto)
+    if (variant_req == kVariantPair || variant_req == kVariantSwapPair || variant_req == kVariantAuto)
         if (int rc = prepare_pair_kernel(*ds))  // also learns how many CTA pairs fit at once
             return rc;
     CachedTable *t = nullptr;
@@ -1067,6 +1433,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     case 1: rc = prepare_kernel<128, 2>(*ds, 1); break;
     case 2: rc = prepare_kernel<256, kDeepStages256>(*ds, 2); break;
     case 3: rc = prepare_kernel<256, 2>(*ds, 3); break;
+    case kVariantSwap: rc = prepare_swap_kernel(*ds); break;
+    case kVariantSwapPair: rc = prepare_swap_pair_kernel(*ds); break;
     default: rc = prepare_pair_kernel(*ds); break;
     }
     if (rc)
@@ -1076,6 +1444,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
     case 1: rc = launch_gemm<128, 2>(*ds, *t, stream, (int)gs.size()); break;
     case 2: rc = launch_gemm<256, kDeepStages256>(*ds, *t, stream, (int)gs.size()); break;
     case 3: rc = launch_gemm<256, 2>(*ds, *t, stream, (int)gs.size()); break;
+    case kVariantSwap: rc = launch_swap(*ds, *t, stream, (int)gs.size()); break;
+    case kVariantSwapPair: rc = launch_swap_pair(*ds, *t, stream, (int)gs.size()); break;
     default: rc = launch_pair(*ds, *t, stream, (int)gs.size()); break;
     }
     if (rc == NVFP4_OK) {
@@ -1251,7 +1621,7 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         g_opt.sf_direct = value;
         return NVFP4_OK;
     case NVFP4_OPT_CTA_PAIR:
-        if (value < 0 || value > 2)
+        if (value < 0 || value > 4)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.cta_pair = value;
         return NVFP4_OK;
@@ -1545,6 +1915,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.workspace = nullptr;  // no split tiles here
     args.counters = nullptr;
     std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
+    fill_param_maps(args, h, (int)ngroups);
     CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages>, (unsigned)grid,
                            Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");

@@ -99,13 +99,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
         first_item = global_item(args, item_begin);
-    // The groups' tensor maps (A, B, and C for the epilogue's stores), fetched ahead
-    // by the producer warp's lanes in parallel: one prefetch.tensormap per lane.
+    // The operand maps of groups past those in the launch parameters, fetched ahead by
+    // the producer warp's lanes in parallel.
     if (warp == kProducerWarp)
-        for (int i = (int)lane; i < 3 * min(args.num_groups, 64); i += 32) {
-            const GroupEntry &g = tab->group(i / 3);
-            tensormap_prefetch(i % 3 == 0 ? &g.tmap_a : i % 3 == 1 ? &g.tmap_b : &g.tmap_c);
-        }
+        prefetch_table_maps(tab, args.num_groups, lane);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
@@ -163,15 +160,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 const int a_map = w.flags >> kItemAMapShift;
                 const GroupEntry &ga = tab->group(a_map);  // the (possibly shared) A map
                 const bool sf_rm_item = (w.flags & kItemSfRowMajor) != 0;
+                // maps read from the table take an acquire fence before their first use
+                const CUtensorMap *tmap_a = map_a(args, tab, a_map), *tmap_b = map_b(args, tab, w.group);
                 if (w.group != fenced_b) {
                     fenced_b = w.group;
-                    tensormap_acquire(&ge.tmap_b);
+                    if (w.group >= kParamMapGroups)
+                        tensormap_acquire(tmap_b);
                     if (sf_rm_item)
                         tensormap_acquire(&ge.tmap_sfb);
                 }
                 if (a_map != fenced_a) {
                     fenced_a = a_map;
-                    tensormap_acquire(&ga.tmap_a);
+                    if (a_map >= kParamMapGroups)
+                        tensormap_acquire(tmap_a);
                     if (sf_rm_item)
                         tensormap_acquire(&ga.tmap_sfa);
                 }
@@ -199,8 +200,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     const uint32_t fb = smem_addr(&full[stage]);
                     mbar_arrive_expect_tx(fb, bytes);
                     if (!(args.fault_skip_load >= 0 && blockIdx.x == 0 && kiter == (uint32_t)args.fault_skip_load)) {
-                        tma_load_2d(slot, &ga.tmap_a, kb * kRowBytes, ya, fb, pol_a);
-                        tma_load_2d(slot + L::kOffB, &ge.tmap_b, kb * kRowBytes, yb, fb, pol_b);
+                        tma_load_2d(slot, tmap_a, kb * kRowBytes, ya, fb, pol_a);
+                        tma_load_2d(slot + L::kOffB, tmap_b, kb * kRowBytes, yb, fb, pol_b);
                         if (sf_rm) {  // K % 256 == 0: a whole stage; B's box is both halves, 256 rows
                             tma_load_2d(slot + L::kOffSfa, &ga.tmap_sfa, kb * kSfRowBytes, ya, fb, pol_a);
                             tma_load_2d(slot + L::kOffSfb, &ge.tmap_sfb, kb * kSfRowBytes, w.tile_n * kPairBlockN, fb,
@@ -347,14 +348,15 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         if (warp == kEpilogueWarp0)
             prefetch_scale_maps(tab, args.num_groups, lane);
         uint32_t acc_phase = 0;
-        int fenced = -1;  // the group whose C map lane 0 last fenced (it issues the stores)
+        int fenced = -1;  // the group whose C map lane 0 (which issues the stores) last fenced
         grid_dependency_wait();  // C and the split workspace may still be in use by the previous kernel
         for (uint32_t it = item_begin; it < item_end; ++it) {
             const WorkItem w = global_item(args, it);
             const GroupEntry &ge = tab->group(w.group);
             const int M = ge.M, N = ge.N;
-            if (lane == 0 && w.group != fenced) {
-                tensormap_acquire(&ge.tmap_c);
+            // before the wait for the accumulator, so that the fence overlaps the MMAs
+            if (lane == 0 && w.group >= kParamMapGroups && w.group != fenced) {
+                tensormap_acquire(map_c(args, tab, w.group));
                 fenced = w.group;
             }
             if (!warp_wait_phase(smem_addr(acc_full), acc_phase, sh, args, kRoleEpilogue, (int)it, -1))
@@ -388,7 +390,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int c = 0; c < kCols / 32; ++c)
                         if (n0 + c * 32 < N)
-                            out.store(&ge.tmap_c, n0 + c * 32, m_row0, h[c], lane);
+                            out.store(map_c(args, tab, w.group), n0 + c * 32, m_row0, h[c], lane);
                 }
             } else {
                 // One segment of a split tile, this CTA's 128 rows. Thread e keeps its
@@ -468,7 +470,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                                     h[2 * f] = pack_half2(__float_as_uint(acc[f].x), __float_as_uint(acc[f].y));
                                     h[2 * f + 1] = pack_half2(__float_as_uint(acc[f].z), __float_as_uint(acc[f].w));
                                 }
-                                out.store(&ge.tmap_c, n0 + c * 32, m_row0, h, lane);
+                                out.store(map_c(args, tab, w.group), n0 + c * 32, m_row0, h, lane);
                             }
                         }
                     }

@@ -152,6 +152,15 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t byt
     asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
 
+// A 32-bit global load with acquire semantics at GPU scope: later loads of this
+// thread see every write that was released before the value it reads.
+__device__ __forceinline__ int ld_acquire_gpu(const int *p)
+{
+    int v;
+    asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
 // ------------------------------------------------------------- L2 policies --
 
 __device__ __forceinline__ uint64_t policy_evict_first()
@@ -173,6 +182,14 @@ __device__ __forceinline__ uint64_t policy_evict_normal()
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
     return p;
+}
+
+// A 16-byte global store with an L2 eviction-priority hint.
+__device__ __forceinline__ void st_global_keep(void *p, uint32_t a, uint32_t b, uint32_t c, uint32_t d, uint64_t policy)
+{
+    asm volatile("st.global.L2::cache_hint.v4.b32 [%0], {%1, %2, %3, %4}, %5;" ::"l"(p), "r"(a), "r"(b), "r"(c), "r"(d),
+                 "l"(policy)
+                 : "memory");
 }
 
 // --------------------------------------------------------------------- TMA --
@@ -381,6 +398,22 @@ __device__ __forceinline__ void tmem_load_16cols(uint32_t taddr, uint32_t (&r)[1
         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
           "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
         : "r"(taddr));
+}
+
+// The same for 8 consecutive columns.
+__device__ __forceinline__ void tmem_load_8cols(uint32_t taddr, uint32_t (&r)[8])
+{
+    asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0, %1, %2, %3, %4, %5, %6, %7}, [%8];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+                 : "r"(taddr));
+}
+
+// Ties 8 registers written by tmem_load_8cols to a point after tmem_load_wait().
+__device__ __forceinline__ void reg_fence(uint32_t (&r)[8])
+{
+    asm volatile("" : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7])
+                 :
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_load_wait()

@@ -112,7 +112,16 @@ struct Table {
 // Tile lists per launch: one per CTA, or per CTA pair.
 constexpr int kMaxLists = 256;
 
+// The A, B and C tensor maps of the first kParamMapGroups groups travel in the launch
+// parameters (param space, read by TMA directly): they need neither a fetch from
+// global memory at start-up nor the acquire fence that a map written by the host into
+// global memory needs before its first use (see tensormap_acquire). 3 KB of
+// parameters; the maps of further groups are read from the table.
+constexpr int kParamMapGroups = 8;
+
 struct KernelArgs {
+    CUtensorMap pmaps[2 * kParamMapGroups];  // A, B of group g at 2g, 2g + 1 (g < min(groups, kParamMapGroups))
+    CUtensorMap cmaps[kParamMapGroups];      // C of group g
     const Table *table;
     const int4 *items;      // the table's work items (four int4 each), so that no read waits for the header
     // List l holds items list_begin[l] .. list_begin[l+1]-1. A copy of the table's

@@ -173,16 +173,27 @@ int nvfp4_last_a_maps(void);
 
 /* Options for tests and tuning. They apply to the calls that follow, are
  * process-wide, and take part in the table cache's key.
- *  NVFP4_OPT_CTA_PAIR      : 0 = automatic, 1 = CTA pairs, 2 = single CTAs.
+ *  NVFP4_OPT_CTA_PAIR      : the kernel kind. 0 = automatic, 1 = CTA pairs, 2 = single
+ *                             CTAs, 3 = swapped operands on single CTAs, 4 = swapped
+ *                             operands on CTA pairs.
  *                             CTA pairs: each cluster of two CTAs computes 256 x 256
  *                             output tiles with the pair form of the MMA (M = 256),
  *                             each SM loading its own 128 A rows and half of the B
- *                             tile. Automatic (when BLOCK_N and STAGES are 0 too):
- *                             per problem set, whichever kind finishes its busiest
- *                             tile list sooner by a measured per-stage cost model
- *                             (pairs for the MoE-sized sets, single CTAs for small
- *                             sets that would leave SMs idle). BLOCK_N and STAGES
- *                             apply to single CTAs only.
+ *                             tile. Swapped operands (swap-AB): the output tile is
+ *                             computed transposed, 128 (single) or 256 (pairs) rows of
+ *                             B on the MMA's M side and the group's rows of A, rounded
+ *                             up to 16, on its N side (up to 2 x 128 per item on single
+ *                             CTAs, 256 on pairs), so a group with few rows wastes no
+ *                             MMA width and loads only the rows it has; their tile
+ *                             lists are cut along K (stream-K) where that shortens the
+ *                             busiest list (SPLIT_TAIL 0 turns that off).
+ *                             Automatic (when BLOCK_N and STAGES are 0 too): swapped
+ *                             operands on single CTAs when every group has at most 32
+ *                             rows of A, else whichever of pairs and single CTAs
+ *                             finishes its busiest tile list sooner by a measured
+ *                             per-stage cost model (pairs for the MoE-sized sets,
+ *                             single CTAs for small sets that would leave SMs idle).
+ *                             BLOCK_N and STAGES apply to unswapped single CTAs only.
  *  NVFP4_OPT_BLOCK_N       : 0 = automatic (128), or 128 or 256: the width of
  *                             the single-CTA output tiles (and the MMA's N)
  *  NVFP4_OPT_STAGES        : 0 = automatic (the deepest shared-memory ring that

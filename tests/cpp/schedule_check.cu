@@ -95,6 +95,91 @@ static void check(const std::vector<ActiveGroup> &gs, int bm, int bn, int cap, b
 
 static ActiveGroup G(int M, int N, int K) { return ActiveGroup{M, N, K, 0, nullptr, nullptr, nullptr, nullptr, nullptr}; }
 
+// The swapped-operand kernel's schedule: items of one 128-row B tile against one or two
+// 128-row A tiles, whole or cut along K (stream-K).
+//  * every (group, B tile, A tile pair) is covered over K exactly once, by segments in K
+//    order, each at least kSwapMinSeg K-stages long when the tile is cut;
+//  * split bookkeeping: one split id per tile with ntok counters, consecutive slots per
+//    segment (ntok each);
+//  * the item's MMA widths and A box follow from M;
+//  * each list walks its items in tile order;
+//  * with stream-K the lists' stage counts differ by at most one tile's worth.
+// Returns the busiest list's shared-memory stages.
+static int64_t check_swap(const std::vector<ActiveGroup> &gs, int cap, bool stream_k)
+{
+    Schedule sc = build_swap_schedule(gs, cap, stream_k);
+    const int G = sc.grid;
+    CHECK(G >= 1 && G <= cap, "grid %d of %d", G, cap);
+    CHECK((int)sc.list_begin.size() == G + 1 && sc.list_begin[G] == sc.items.size(), "lists");
+    std::map<std::tuple<int, int, int>, std::vector<WorkItem>> by_tile;
+    std::vector<int64_t> load(G, 0);
+    int64_t max_tile = 0;
+    int splits = 0, slots = 0;
+    bool any_split = false;
+    for (int l = 0; l < G; ++l) {
+        CHECK(sc.list_begin[l] <= sc.list_begin[l + 1], "monotone");
+        std::tuple<int, int, int> prev{-1, -1, -1};
+        for (uint32_t i = sc.list_begin[l]; i < sc.list_begin[l + 1]; ++i) {
+            const WorkItem &w = sc.items[i];
+            const std::tuple<int, int, int> key{w.group, w.tile_n, w.tile_m};
+            CHECK(prev < key, "list %d not in tile order", l);
+            prev = key;
+            by_tile[{w.group, w.tile_n, w.tile_m}].push_back(w);
+            const int ntok = swap_ntok(w.flags);
+            load[l] += (int64_t)(w.kb_end - w.kb_begin) * ntok;
+            CHECK(w.kb_end > w.kb_begin, "empty segment");
+            any_split = any_split || w.split >= 0;
+        }
+    }
+    size_t tiles = 0;
+    for (size_t g = 0; g < gs.size(); ++g) {
+        const int M = gs[g].M, ntt = (M + 127) / 128, tw = (gs[g].N + 127) / 128, nk = (gs[g].K / 64 + 3) / 4;
+        for (int wt = 0; wt < tw; ++wt)
+            for (int t0 = 0; t0 < ntt; t0 += 2) {
+                ++tiles;
+                auto it = by_tile.find({(int)g, wt, t0});
+                CHECK(it != by_tile.end(), "tile missing g=%zu w=%d t0=%d", g, wt, t0);
+                if (it == by_tile.end())
+                    continue;
+                auto segs = it->second;
+                std::sort(segs.begin(), segs.end(), [](const WorkItem &a, const WorkItem &b) { return a.seg < b.seg; });
+                const int ntok = std::min(2, ntt - t0);
+                max_tile = std::max<int64_t>(max_tile, (int64_t)nk * ntok);
+                int k = 0;
+                for (size_t j = 0; j < segs.size(); ++j) {
+                    const WorkItem &w = segs[j];
+                    CHECK(swap_ntok(w.flags) == ntok, "ntok");
+                    CHECK(swap_nt(w.flags, 0) == round16(std::min(128, M - 128 * t0)), "nt0");
+                    CHECK(ntok == 1 || swap_nt(w.flags, 1) == round16(std::min(128, M - 128 * (t0 + 1))), "nt1");
+                    CHECK(swap_box_rows(w.flags) == (M <= 128 ? round16(M) : 128), "box");
+                    CHECK(w.a_row == 128 * t0 && w.tile_m == t0, "a rows");
+                    CHECK(w.seg == (int)j && w.nseg == (int)segs.size(), "seg numbering");
+                    CHECK(w.kb_begin == k, "gap or overlap at k=%d", k);
+                    k = w.kb_end;
+                    if (segs.size() > 1) {
+                        CHECK(w.kb_end - w.kb_begin >= kSwapMinSeg, "segment of %d stages", w.kb_end - w.kb_begin);
+                        CHECK(w.split == segs[0].split && w.ws_slot == segs[0].ws_slot + (int)j * ntok, "split bookkeeping");
+                    } else {
+                        CHECK(w.split == -1, "whole tile marked split");
+                    }
+                }
+                CHECK(k == nk, "K not covered: %d of %d", k, nk);
+                if (segs.size() > 1) {
+                    splits += ntok;
+                    slots += (int)segs.size() * ntok;
+                }
+            }
+    }
+    CHECK(by_tile.size() == tiles, "extra tiles");
+    CHECK(sc.splits == splits && sc.ws_slots == slots, "split counts %d/%d slots %d/%d", sc.splits, splits, sc.ws_slots,
+          slots);
+    CHECK(stream_k || !any_split, "split with stream-K off");
+    const int64_t mx = *std::max_element(load.begin(), load.end()), mn = *std::min_element(load.begin(), load.end());
+    if (any_split)
+        CHECK(mx - mn <= max_tile, "stream-K imbalance %lld..%lld", (long long)mn, (long long)mx);
+    return mx;
+}
+
 int main()
 {
     std::vector<std::vector<ActiveGroup>> sets = {
@@ -116,6 +201,72 @@ int main()
             for (int cap : {152, 148, 76, 40, 7, 1})
                 for (bool split : {true, false})
                     check(gs, sh[0], sh[1], cap, split);
+    for (auto &gs : sets)
+        for (int cap : {152, 148, 76, 40, 7, 1})
+            for (bool sk : {true, false})
+                check_swap(gs, cap, sk);
+    // the CTA-pair swapped kernel's schedule: tiles of 256 rows of B x up to 256 rows of A,
+    // covered over K exactly once, split bookkeeping consistent, lists in tile order
+    for (auto &gs : sets)
+        for (int cap : {76, 40, 7, 1})
+            for (bool sk : {true, false}) {
+                const Schedule sc = build_swap_pair_schedule(gs, cap, sk);
+                CHECK(sc.grid >= 1 && sc.grid <= cap && sc.list_begin[sc.grid] == sc.items.size(), "pair lists");
+                std::map<std::tuple<int, int, int>, std::vector<WorkItem>> by_tile;
+                int splits = 0, slots = 0;
+                for (int l = 0; l < sc.grid; ++l) {
+                    std::tuple<int, int, int> prev{-1, -1, -1};
+                    for (uint32_t i = sc.list_begin[l]; i < sc.list_begin[l + 1]; ++i) {
+                        const WorkItem &w = sc.items[i];
+                        const std::tuple<int, int, int> key{w.group, w.tile_n, w.tile_m};
+                        CHECK(prev < key, "pair list %d order", l);
+                        prev = key;
+                        by_tile[key].push_back(w);
+                        CHECK(swap_pair_nt(w.flags) == round16(std::min(gs[w.group].M, 256)), "pair nt");
+                    }
+                }
+                size_t tiles = 0;
+                for (size_t g = 0; g < gs.size(); ++g) {
+                    const int nk = (gs[g].K / 64 + 3) / 4;
+                    for (int wt = 0; wt < (gs[g].N + 255) / 256; ++wt)
+                        for (int t = 0; t < (gs[g].M + 255) / 256; ++t) {
+                            ++tiles;
+                            auto segs = by_tile[{(int)g, wt, t}];
+                            std::sort(segs.begin(), segs.end(),
+                                      [](const WorkItem &a, const WorkItem &b) { return a.seg < b.seg; });
+                            int k = 0;
+                            for (size_t j = 0; j < segs.size(); ++j) {
+                                CHECK(segs[j].kb_begin == k && segs[j].seg == (int)j, "pair coverage");
+                                k = segs[j].kb_end;
+                                if (segs.size() > 1)
+                                    CHECK(segs[j].ws_slot == segs[0].ws_slot + (int)j && segs[j].split == segs[0].split,
+                                          "pair split bookkeeping");
+                            }
+                            CHECK(k == nk, "pair K coverage");
+                            if (segs.size() > 1) {
+                                splits += 1;
+                                slots += (int)segs.size();
+                            }
+                        }
+                }
+                CHECK(by_tile.size() == tiles && sc.splits == splits && sc.ws_slots == slots, "pair counts");
+            }
+    // the K = 7168 MoE set goes stream-K on 152 SMs (whole items would leave a short last
+    // wave); the K = 2048 set's whole items already balance within a stage or two. Both
+    // stay within a few stages of the even share.
+    CHECK(build_swap_schedule(sets[0], 152, true).splits > 0, "moe K=7168: stream-K");
+    for (int i = 0; i < 2; ++i) {
+        const Schedule sc = build_swap_schedule(sets[i], 152, true);
+        CHECK(sc.grid == 152, "moe set %d: grid %d", i, sc.grid);
+        const int64_t mx = check_swap(sets[i], 152, true);
+        int64_t total = 0;
+        for (const WorkItem &w : sc.items)
+            total += (int64_t)(w.kb_end - w.kb_begin) * swap_ntok(w.flags);
+        CHECK(mx <= (total + 151) / 152 + 2 * kSwapMinSeg, "moe set %d: busiest list %lld of %lld", i, (long long)mx,
+              (long long)total);
+        std::printf("swap-AB moe set %d: %lld stages over 152 CTAs, busiest %lld, %d split tiles\n", i, (long long)total,
+                    (long long)mx, sc.splits);
+    }
     // the two MoE sets split at both tile widths, and the K=2048 set at width 128 does not
     auto splits = [](const std::vector<ActiveGroup> &gs, int bn) {
         Schedule sc = build_schedule(gs, 128, bn, 152, true);
@@ -159,6 +310,11 @@ int main()
         CHECK(choose_variant(g2a, ds, 0, 1) == 0, "g2 K=1536 -> single");
         CHECK(choose_variant(g2b, ds, 0, 1) == 0, "g2 K=4096 -> single");
         CHECK(choose_variant(tiny, ds, 0, 1) == 0, "tiny -> single");
+        // decode-sized sets (every group at most 32 rows of A): the swapped-operand kernel
+        const std::vector<ActiveGroup> dec = {G(8, 4096, 7168), G(32, 4096, 7168), G(1, 4096, 7168)};
+        CHECK(choose_variant(dec, ds, 0, 1) == kVariantSwap, "decode -> swap-AB");
+        const std::vector<ActiveGroup> mid = {G(33, 4096, 7168), G(8, 4096, 7168)};
+        CHECK(choose_variant(mid, ds, 0, 1) != kVariantSwap, "33 rows -> not swap-AB");
     }
     // M-fusion runs (a_runs): A rows that follow one another with the same K join the
     // previous group's run; a gap, a change of K or of the scale layout, row-major SFA rows

@@ -55,6 +55,15 @@ def test_prepack_bitwise(rows, K):
 
 # ------------------------------------------------------------ small, full ---
 
+def test_decode_sized_sets_take_the_swapped_kernel():
+    # every group at most 32 rows of A: the automatic choice is the swapped-operand kernel
+    groups = gen.make_problem_set(11, [8, 16, 4, 32, 1, 3], [4096, 512, 1024, 136, 8, 264], [7168, 256, 1024, 2048, 64, 448])
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    assert nv.nvfp4_last_kernel() == "nvfp4_swapab_gemm_kernel<5>"
+    check_full(groups, d, "decode-sized set")
+
+
 def test_tiny_workload_every_output():
     groups = gen.make_workload("tiny_g2")
     d = [DeviceGroup(g) for g in groups]
@@ -316,12 +325,15 @@ def test_two_streams_at_once_with_split_tails():
 # ------------------------------------------------------- full-size, every output ---
 
 @pytest.mark.parametrize("pair,layout", [(0, nv.NVFP4_SF_PREPACKED), (1, nv.NVFP4_SF_ROWMAJOR),
-                                         (2, nv.NVFP4_SF_PREPACKED), (2, nv.NVFP4_SF_ROWMAJOR)])
+                                         (2, nv.NVFP4_SF_PREPACKED), (2, nv.NVFP4_SF_ROWMAJOR),
+                                         (3, nv.NVFP4_SF_PREPACKED), (3, nv.NVFP4_SF_ROWMAJOR),
+                                         (4, nv.NVFP4_SF_PREPACKED), (4, nv.NVFP4_SF_ROWMAJOR)])
 @pytest.mark.parametrize("name", ["g2_n4096_k1536", "g2_n3072_k4096", "moe_g8_n7168_k2048", "moe_g8_n4096_k7168"])
 def test_full_size_workloads_every_output(name, pair, layout):
     # pair 0: the automatic choice with prepacked scales, the benchmark's launch
     # configuration; 1: CTA pairs; 2: single CTAs (which split the MoE sets' last
-    # wave along K). Row-major scales are read in the kernel (the e2e benchmark's route).
+    # wave along K); 3 and 4: the swapped-operand kernels, single CTAs and CTA pairs
+    # (stream-K). Row-major scales are read in the kernel (the e2e benchmark's route).
     # Every output is compared with the oracle's.
     nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
     groups = gen.make_workload(name)

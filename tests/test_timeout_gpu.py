@@ -28,7 +28,7 @@ pytestmark = pytest.mark.gpu
 CASES = [([128], [128], [4096]), ([64, 128], [512, 512], [512, 512])]
 
 
-@pytest.mark.parametrize("pair", [1, 2])
+@pytest.mark.parametrize("pair", [1, 2, 3, 4])
 @pytest.mark.parametrize("Ms,Ns,Ks", CASES)
 def test_wait_timeout_reports_and_recovers(Ms, Ns, Ks, pair):
     groups = gen.make_problem_set(1, Ms, Ns, Ks)
