@@ -36,7 +36,10 @@ Timing (ours):
    every 5 ms through NVML during the timed region.
  * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
    scaling; the path has no exchange step). Timing is the max over ranks, and
-   `value` = that time divided by N (aggregate time per grouped call).
+   `value` = that time divided by N (aggregate time per grouped call). With
+   --split groups|n the ranks instead share ONE call (strong scaling): whole
+   groups, or N ranges of every group, each rank writing its own outputs (C stays
+   sharded, nothing crosses between ranks); `value` = the slowest rank's time.
 --impl reference times the CPU oracle (the plain C reference restated from the
 pages) on bounded samples of the same workload.
 """
@@ -410,6 +413,18 @@ def time_cold_calls(keep, stream, flush, reps):
     return out
 
 
+def shard_inputs(groups, world, rank, mode):
+    """This rank's share of one call (block_scaled_fp4_persistent_gb300.shard's plans) as
+    host inputs: whole groups, or every group cut to this rank's range of B's rows (and
+    its scale rows); the rank's C is its column block of each group's C."""
+    from block_scaled_fp4_persistent_gb300 import shard
+    shapes = [(g.M, g.N, g.K) for g in groups]
+    if mode == "groups":
+        return [groups[i] for i in shard.shard_groups(shapes, world)[rank]]
+    return [gen.GroupInputs(groups[gi].M, n1 - n0, groups[gi].K, groups[gi].A, groups[gi].B[n0:n1], groups[gi].SFA,
+                            groups[gi].SFB[n0:n1]) for gi, n0, n1 in shard.shard_n(shapes, world)[rank]]
+
+
 def run_ours(args, groups, rank, world, local_rank):
     import torch
     import block_scaled_fp4_persistent_gb300 as nv
@@ -589,15 +604,17 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
     roof_us = max(t_fp4_us, t_hbm_us)
     out = {
         "metric": "us per grouped call (NVFP4 block-scaled grouped GEMM, fp16 out)",
-        "value": round(mean_us_all / world, 3),
+        # replicas: N calls finish in the slowest rank's time, so one call costs that / N;
+        # shards: one call finishes in the slowest rank's time
+        "value": round(mean_us_all / (world if args.split == "replicas" else 1), 3),
         "unit": "us",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
         "ms_per_step": round(mean_us_all / 1e3, 6),
         "higher_is_better": False,
-        "scaling": "weak",
-        "vs_baseline": (round(mean_us_all / world / PAGES_BEST_US[args.workload], 4)
+        "scaling": "weak" if args.split == "replicas" else "strong",
+        "vs_baseline": (round(mean_us_all / (world if args.split == "replicas" else 1) / PAGES_BEST_US[args.workload], 4)
                         if args.workload in PAGES_BEST_US else None),
         "vs_baseline_ref": ({"value": PAGES_BEST_US[args.workload], "unit": "us", "hardware": "B200",
                              "what": "the pages' best leaderboard time for this workload (context, not the target)"}
@@ -608,7 +625,8 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
                    "N": [g.N for g in groups], "K": [g.K for g in groups], "seed": gen.WORKLOADS[args.workload]["seed"],
                    "kernel_choice": args.kernel,
                    "scales": "prepacked 128x4 blocked layout", "l2": "flushed before every timed call "
-                   "(2xL2 write, then 2xL2 read)", "parallelism": f"replicas x{world}"},
+                   "(2xL2 write, then 2xL2 read)", "parallelism": (f"replicas x{world}" if args.split == "replicas"
+                                   else f"one call in {args.split} shards x{world} (rank 0's share below)")},
         "median_us": round(med_us, 3),
         "min_us": round(min(per_call_ms) * 1e3, 3),
         "max_us": round(max(per_call_ms) * 1e3, 3),
@@ -630,11 +648,13 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
         "clocks": clocks.summary(),
         "prepack": prepack,
         "cold_call": cold,
-        "chained": {"value": round(chain_us / world, 3), "unit": "us", "calls_per_batch": chain_calls,
+        "chained": {"value": round(chain_us / (world if args.split == "replicas" else 1), 3), "unit": "us",
+                    "calls_per_batch": chain_calls,
                     "batches": chain_batches, "pdl": True,
                     "l2": ("flushed before each batch only; one call's inputs and C (%.0f MB) %s L2 (%.0f MB)"
                            % (working_set / 1e6, "exceed" if working_set > l2 else "fit in", l2 / 1e6))},
-        "e2e": {"value": round(e2e_us / world, 3), "unit": "us", "steps": e2e_steps, "h2d_bytes_per_step": h2d,
+        "e2e": {"value": round(e2e_us / (world if args.split == "replicas" else 1), 3), "unit": "us", "steps": e2e_steps,
+                "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "gpu_launches_per_step": e2e_launches,
                 "path": "one pinned host arena of A/B/row-major SFA/SFB -> one H2D copy -> nvfp4_grouped_gemm (the GEMM "
                         "kernel reads the row-major scales itself where K % 256 == 0, else a prepack launch first) -> "
@@ -695,6 +715,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="moe_g8_n4096_k7168", choices=sorted(gen.WORKLOADS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--split", default="replicas", choices=["replicas", "groups", "n"],
+                    help="N > 1: every rank runs its own replica of the call (weak scaling, the default), or "
+                         "its share of ONE call: whole groups, or N ranges of every group (strong scaling)")
     ap.add_argument("--kernel", default="auto", choices=sorted(KERNEL_CHOICE),
                     help="kernel kind (NVFP4_OPT_CTA_PAIR): the library's automatic choice by default")
     ap.add_argument("--e2e-steps", type=int, default=100)
@@ -754,8 +777,12 @@ def main():
     if args.kernel != "auto":
         import block_scaled_fp4_persistent_gb300 as nv
         nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, KERNEL_CHOICE[args.kernel])
-    # each rank draws its own replica of the workload (weak scaling)
-    groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
+    if args.split == "replicas":
+        # each rank draws its own replica of the workload (weak scaling)
+        groups = gen.make_problem_set(w["seed"] + rank, w["Ms"], w["Ns"], w["Ks"])
+    else:
+        # every rank draws the same call and runs its share of it (strong scaling)
+        groups = shard_inputs(gen.make_problem_set(w["seed"], w["Ms"], w["Ns"], w["Ks"]), world, rank, args.split)
     out = run_ours(args, groups, rank, world, local_rank)
     if world == 1 and args.workload == "moe_g8_n4096_k7168" and not args.no_other_workloads:
         # the other workloads, timed the same way (not part of the headline value)

@@ -64,6 +64,8 @@ class Nvfp4Problem(ctypes.Structure):
         ("A", ctypes.c_void_p), ("B", ctypes.c_void_p),
         ("SFA", ctypes.c_void_p), ("SFB", ctypes.c_void_p),
         ("C", ctypes.c_void_p),
+        ("ldc", ctypes.c_int32),       # elements between rows of C; 0 means N
+        ("reserved", ctypes.c_int32),
     ]
 
 
@@ -213,12 +215,14 @@ def nvfp4_release() -> None:
 
 def problem(A, B, SFA, SFB, C, sf_layout: int = NVFP4_SF_PREPACKED) -> Nvfp4Problem:
     """An Nvfp4Problem from CUDA tensors. A: uint8 [M, K/2]; B: uint8 [N, K/2];
-    SFA/SFB: uint8 scale bytes in `sf_layout`; C: fp16 [M, N]. The caller keeps
+    SFA/SFB: uint8 scale bytes in `sf_layout`; C: fp16 [M, N], dense, or a column
+    block of a wider row-major matrix (its row stride becomes ldc). The caller keeps
     the tensors alive until the launch has run."""
     M, N = C.shape
     K = A.shape[1] * 2 if A.dim() == 2 else 0
+    ldc = 0 if C.stride(0) == N else C.stride(0)
     return Nvfp4Problem(M, N, K, sf_layout, A.data_ptr(), B.data_ptr(), SFA.data_ptr(), SFB.data_ptr(),
-                        C.data_ptr())
+                        C.data_ptr(), ldc, 0)
 
 
 def prepack_scales(sf_rowmajor, K: int, out=None, stream=None):

@@ -42,8 +42,8 @@ typedef struct CUstream_st *nvfp4_stream_t;
 
 enum {
     NVFP4_OK = 0,
-    NVFP4_ERR_INVALID_ARG = -1,        /* g < 0, NULL probs, negative sizes, NULL pointer of a non-empty operand, bad sf_layout */
-    NVFP4_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, K % 64 != 0, or N % 8 != 0 */
+    NVFP4_ERR_INVALID_ARG = -1,        /* g < 0, NULL probs, negative sizes, NULL pointer of a non-empty operand, bad sf_layout, 0 < ldc < N, reserved != 0 */
+    NVFP4_ERR_ALIGNMENT = -2,          /* a pointer not 16-byte aligned, K % 64 != 0, N % 8 != 0 or ldc % 8 != 0 */
     NVFP4_ERR_UNSUPPORTED_DEVICE = -3, /* current device is not compute capability 10.3 (sm_103a) */
     NVFP4_ERR_CUDA = -4,               /* a CUDA runtime or driver call failed; see nvfp4_last_cuda_error() */
     NVFP4_ERR_TIMEOUT = -5,            /* a kernel gave up a bounded wait; reported by nvfp4_device_status() */
@@ -77,7 +77,14 @@ enum {
  *  SFA, SFB : E4M3 scale bytes, one per 16 consecutive K of a row, in the layout
  *             sf_layout names. The scale type the tensor core reads is unsigned
  *             (UE4M3), so the sign bit must be 0. 0x7F is NaN and not allowed.
- *  C        : [M][N] fp16, row-major, ldc = N. Only m < M and n < N are written.
+ *  C        : [M][N] fp16, row-major, rows ldc elements apart. Only m < M and n < N
+ *             are written.
+ *  ldc      : elements between consecutive rows of C. 0 means N (the pages' layout, a
+ *             dense C). A library extension, for writing a column block of a wider
+ *             matrix (e.g. one GPU's N-range of a call that is split across GPUs): then
+ *             ldc >= N, ldc % 8 == 0 (16-byte rows), and C points at the block's first
+ *             element.
+ *  reserved : must be 0.
  *  A, B, SFA, SFB and C must be 16-byte aligned. */
 typedef struct {
     int32_t M, N, K;
@@ -87,6 +94,8 @@ typedef struct {
     const void *SFA;
     const void *SFB;
     void *C;
+    int32_t ldc;
+    int32_t reserved;
 } Nvfp4Problem;
 
 /* The grouped GEMM: one persistent kernel launch for all g problems (plus a
