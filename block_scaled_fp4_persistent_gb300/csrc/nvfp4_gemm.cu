@@ -63,8 +63,8 @@ struct Options {
 // programmatic stream serialization: the kernel may start (set up barriers and
 // TMEM, read its own tables) while the previous kernel in the stream finishes;
 // it waits for that kernel before it reads or writes the caller's memory.
-template <class Kernel>
-cudaError_t launch_kernel(Kernel kernel, unsigned grid, size_t smem, cudaStream_t stream, const KernelArgs &args)
+template <class Kernel, class Args>
+cudaError_t launch_kernel(Kernel kernel, unsigned grid, size_t smem, cudaStream_t stream, const Args &args)
 {
     if (g_opt.pdl.load() == 0) {
         kernel<<<grid, kThreads, smem, stream>>>(args);
@@ -1238,10 +1238,21 @@ int prepare_pair_kernel(DeviceState &ds)
     return NVFP4_OK;
 }
 
+// Each list's first item, copied from the table's host copy into the launch parameters.
+void fill_first_items(PairArgs &args, const CachedTable &t)
+{
+    const TableHeader *th = static_cast<const TableHeader *>(t.host);
+    const WorkItem *items = reinterpret_cast<const WorkItem *>(static_cast<const uint8_t *>(t.host) + th->off_items);
+    const int lists = (int)t.list_begin.size() - 1;
+    for (int l = 0; l < std::min(lists, kParamFirstItems); ++l)
+        if (t.list_begin[l] < t.list_begin[l + 1])
+            args.first[l] = first_item_of(items[t.list_begin[l]]);
+}
+
 int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
 {
     using L = PairLayout<kPairStages>;
-    KernelArgs args{};
+    PairArgs args{};
     args.table = static_cast<const Table *>(t.dev);
     args.items = table_items(t);
     args.status = ds.status;
@@ -1253,6 +1264,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.counters = t.counters;
     fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
+    fill_first_items(args, t);
     CUDA_TRY(launch_kernel(nvfp4_pair_gemm_kernel<kPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_pair_gemm_kernel<5>");
     return NVFP4_OK;
@@ -1312,7 +1324,7 @@ int prepare_swap_pair_kernel(DeviceState &ds)
 int launch_swap_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
 {
     using L = SwapPairLayout<kSwapPairStages>;
-    KernelArgs args{};
+    PairArgs args{};
     args.table = static_cast<const Table *>(t.dev);
     args.items = table_items(t);
     args.status = ds.status;
@@ -1324,6 +1336,7 @@ int launch_swap_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream,
     args.counters = t.counters;
     fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
+    fill_first_items(args, t);
     CUDA_TRY(launch_kernel(nvfp4_swapab_pair_kernel<kSwapPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     static_assert(kSwapPairStages == 5, "kernel name below");
     g_last_kernel.store("nvfp4_swapab_pair_kernel<5>");

@@ -71,7 +71,7 @@ struct PairLayout {
 
 template <int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    nvfp4_pair_gemm_kernel(const __grid_constant__ KernelArgs args)
+    nvfp4_pair_gemm_kernel(const __grid_constant__ PairArgs args)
 {
     using L = PairLayout<STAGES>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -98,7 +98,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     // overlaps the set-up below.
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
-        first_item = global_item(args, item_begin);
+        first_item = pair < kParamFirstItems ? item_of(args.first[pair]) : global_item(args, item_begin);
     // The operand maps of groups past those in the launch parameters, fetched ahead by
     // the producer warp's lanes in parallel.
     if (warp == kProducerWarp)

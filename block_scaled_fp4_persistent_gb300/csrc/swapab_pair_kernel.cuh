@@ -63,7 +63,7 @@ struct SwapPairLayout {
 
 template <int STAGES>
 __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    nvfp4_swapab_pair_kernel(const __grid_constant__ KernelArgs args)
+    nvfp4_swapab_pair_kernel(const __grid_constant__ PairArgs args)
 {
     using L = SwapPairLayout<STAGES>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -88,7 +88,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const uint32_t item_end = args.list_begin[pair + 1];
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
-        first_item = global_item(args, item_begin);
+        first_item = pair < kParamFirstItems ? item_of(args.first[pair]) : global_item(args, item_begin);
     if (warp == kProducerWarp)
         prefetch_table_maps(tab, args.num_groups, lane);
 

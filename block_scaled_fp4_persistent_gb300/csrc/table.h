@@ -136,4 +136,34 @@ struct KernelArgs {
     int *counters;            // per split tile: segments finished so far (0 between launches)
 };
 
+// The fields of a list's first work item that the TMA producer needs for its first
+// copies, in the CTA-pair kernels' launch parameters: the producer's first copy then
+// waits for no load from the (cold) table. 48 bytes a list.
+struct FirstItem {
+    int32_t group, tile_m, tile_n, kb_begin, kb_end, kblocks64, flags, a_row;
+    const uint8_t *sfa;
+    const uint8_t *sfb;
+};
+constexpr int kParamFirstItems = 80;  // lists (CTA pairs) whose first item travels in the parameters
+
+struct PairArgs : KernelArgs {
+    FirstItem first[kParamFirstItems];
+};
+
+__host__ __device__ inline FirstItem first_item_of(const WorkItem &w)
+{
+    return FirstItem{w.group, w.tile_m, w.tile_n, w.kb_begin, w.kb_end, w.kblocks64, w.flags, w.a_row, w.sfa, w.sfb};
+}
+
+// A work item with the fields a FirstItem carries (the split fields are those of a whole tile;
+// the producer does not read them).
+__host__ __device__ inline WorkItem item_of(const FirstItem &f)
+{
+    WorkItem w{};
+    w.group = f.group, w.tile_m = f.tile_m, w.tile_n = f.tile_n, w.kb_begin = f.kb_begin, w.kb_end = f.kb_end;
+    w.split = -1, w.nseg = 1, w.kblocks64 = f.kblocks64, w.flags = f.flags, w.a_row = f.a_row;
+    w.sfa = f.sfa, w.sfb = f.sfb;
+    return w;
+}
+
 }  // namespace nvfp4
