@@ -30,8 +30,11 @@ Timing (ours):
    (--no-other-workloads skips them).
  * Outside the timed region: `prepack` (every SFA and SFB of the workload through
    nvfp4_prepack_scales_batch, one launch, L2 flushed before each call, with its
-   bytes and roofline fraction) and `cold_call` (calls that miss the table cache,
-   against calls that hit it).
+   bytes and roofline fraction; the same launch over one scale row after a flush,
+   the fixed cost of any flushed call; and `chained`: back-to-back calls over
+   rotating operand sets larger than L2 from one CUDA graph, beside a plain
+   device-to-device copy of the same bytes) and `cold_call` (calls that miss the
+   table cache, against calls that hit it).
  * `clocks`: SM clock, power and clock-event reasons of the GPU in use, sampled
    every 5 ms through NVML during the timed region.
  * Under torchrun (N > 1) every rank runs its own replica on its own GPU (weak
@@ -368,10 +371,86 @@ def time_prepack(groups, dev, stream, flush, steps, peaks):
     read = sum(r * k // 16 for r, k in zip(rows, Ks))
     written = sum(nv.nvfp4_prepacked_scale_bytes(r, k) for r, k in zip(rows, Ks))
     gbs = (read + written) / (us * 1e-6) / 1e9
+
+    # the fixed cost of any flushed call: the same launch over one 16-byte scale row
+    one_src = torch.zeros(16, dtype=torch.uint8, device=dev)
+    one_dst = torch.empty(512, dtype=torch.uint8, device=dev)
+    one = ([one_src.data_ptr()], [1], [64], [one_dst.data_ptr()])
+    ev1 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for e0, e1 in ev1:
+        flush()
+        e0.record(stream)
+        nv.nvfp4_prepack_scales_batch(*one, stream)
+        e1.record(stream)
+    torch.cuda.synchronize()
+    floor_us = statistics.fmean(a.elapsed_time(b) for a, b in ev1) * 1e3
+
+    # chained: back-to-back calls over rotating operand sets that together exceed L2 three
+    # times (so each call reads its operands from HBM), captured once in a CUDA graph so that
+    # the host's launch cost does not starve the GPU; beside it, a plain device-to-device copy
+    # of the same read bytes under the same conditions
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    n_sets = max(2, -(-3 * l2 // max(1, read + written)))
+    sets = [args]
+    held = []
+    for _ in range(n_sets - 1):
+        s_src = [t.clone() for t in srcs]
+        s_dst = [torch.empty_like(t) for t in dsts]
+        held.append((s_src, s_dst))
+        sets.append(([t.data_ptr() for t in s_src], rows, Ks, [t.data_ptr() for t in s_dst]))
+    words = read // 4
+    copies = [(torch.empty(words, dtype=torch.int32, device=dev), torch.empty(words, dtype=torch.int32, device=dev))
+              for _ in range(n_sets)]
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+
+    def chained(body):
+        with torch.cuda.stream(side):
+            body()
+        torch.cuda.synchronize()
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph, stream=side):
+            body()
+        for _ in range(3):
+            graph.replay()
+        torch.cuda.synchronize()
+        per = []
+        for _ in range(20):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            with torch.cuda.stream(side):
+                e0.record(side)
+                graph.replay()
+                e1.record(side)
+            torch.cuda.synchronize()
+            per.append(e0.elapsed_time(e1) * 1e3 / n_sets)
+        return statistics.fmean(per)
+
+    def prepack_all():
+        for a in sets:
+            nv.nvfp4_prepack_scales_batch(*a, side.cuda_stream)
+
+    def copy_all():
+        for a, b in copies:
+            b.copy_(a)
+
+    chained_us = chained(prepack_all)
+    copy_us = chained(copy_all)
+    torch.cuda.synchronize()
+    for (_, s_dst) in held:
+        for a, b in zip(s_dst, dsts):
+            if not torch.equal(a, b):
+                raise RuntimeError("chained prepack differs from the timed one")
+    cgbs = (read + written) / (chained_us * 1e-6) / 1e9
     return {"value": round(us, 3), "unit": "us", "steps": steps, "operands": len(rows), "launches": 1,
             "algorithmic_bytes": read + written, "read_bytes": read, "written_bytes": written,
             "achieved_gbs": round(gbs, 1), "frac": round(gbs / peaks["hbm_gbs"], 4),
-            "what": "nvfp4_prepack_scales_batch of every SFA and SFB of the workload, L2 flushed before each call"}
+            "what": "nvfp4_prepack_scales_batch of every SFA and SFB of the workload, L2 flushed before each call",
+            "flushed_floor_us": round(floor_us, 3),
+            "chained": {"value": round(chained_us, 3), "unit": "us", "achieved_gbs": round(cgbs, 1),
+                        "frac": round(cgbs / peaks["hbm_gbs"], 4), "sets": n_sets,
+                        "copy_same_bytes_us": round(copy_us, 3),
+                        "what": f"back-to-back calls over {n_sets} operand sets (together 3x L2), one CUDA graph; "
+                                f"copy_same_bytes_us: a device-to-device copy of the {read} read bytes, same conditions"}}
 
 
 def time_cold_calls(keep, stream, flush, reps):

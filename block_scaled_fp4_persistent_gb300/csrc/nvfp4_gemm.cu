@@ -1432,8 +1432,8 @@ extern "C" int nvfp4_grouped_gemm(int g, const Nvfp4Problem *probs, nvfp4_stream
             if (ws_off[i].first == SIZE_MAX)
                 continue;
             ActiveGroup &a = gs[i];
-            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFA), base + ws_off[i].first, a.M, a.K / 16, 0, 0, 0});
-            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFB), base + ws_off[i].second, a.N, a.K / 16, 0, 0, 0});
+            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFA), base + ws_off[i].first, a.M, a.K / 16, 0, 0, 0, 0});
+            jobs.push_back(PrepackJob{static_cast<const uint8_t *>(a.SFB), base + ws_off[i].second, a.N, a.K / 16, 0, 0, 0, 0});
             a.SFA = base + ws_off[i].first;
             a.SFB = base + ws_off[i].second;
         }
@@ -1513,7 +1513,7 @@ extern "C" int nvfp4_prepack_scales(const void *sf_rowmajor, int rows, int K, vo
         if (int rc = device_state(dev, &ds))
             return rc;
     }
-    PrepackJob j{static_cast<const uint8_t *>(sf_rowmajor), static_cast<uint8_t *>(sf_blocked), rows, K / 16, 0, 0, 0};
+    PrepackJob j{static_cast<const uint8_t *>(sf_rowmajor), static_cast<uint8_t *>(sf_blocked), rows, K / 16, 0, 0, 0, 0};
     CUDA_TRY(launch_prepack(&j, 1, reinterpret_cast<cudaStream_t>(stream)));
     return NVFP4_OK;
 }
@@ -1541,7 +1541,7 @@ extern "C" int nvfp4_prepack_scales_batch(int n, const void *const *sf_rowmajor,
         if (!aligned16(sf_rowmajor[i]) || !aligned16(sf_blocked[i]))
             return NVFP4_ERR_ALIGNMENT;
         jobs.push_back(PrepackJob{static_cast<const uint8_t *>(sf_rowmajor[i]), static_cast<uint8_t *>(sf_blocked[i]),
-                                  rows[i], K[i] / 16, 0, 0, 0});
+                                  rows[i], K[i] / 16, 0, 0, 0, 0});
     }
     if (jobs.empty())
         return NVFP4_OK;

@@ -12,13 +12,14 @@ struct PrepackJob {
     int32_t rows;
     int32_t cols;        // K / 16
     int32_t col_blocks;  // ceil(cols / 4): 512-byte blocks per 128-row tile
-    int32_t chunks;      // ceil(col_blocks / 8): CTAs per 128-row tile
-    int32_t cta_begin;   // first CTA of this job within the launch
+    int32_t units;       // warp work items per 128-row tile: 32 source columns each (16 on the byte path)
+    int32_t item_begin;  // first work item of this job within the launch
+    int32_t vec;         // 1: 16-byte loads (cols % 16 == 0 and src 16-byte aligned); 0: byte loads
 };
 
 constexpr int kPrepackMaxJobs = 32;
 
-// Fills in col_blocks/chunks/cta_begin and launches one kernel for up to
+// Fills in col_blocks/units/item_begin/vec and launches one kernel for up to
 // kPrepackMaxJobs jobs (more are split into several launches).
 cudaError_t launch_prepack(PrepackJob *jobs, int n, cudaStream_t stream);
 

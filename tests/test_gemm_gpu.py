@@ -53,6 +53,29 @@ def test_prepack_bitwise(rows, K):
     assert np.array_equal(out.cpu().numpy()[:ref.size], ref)
 
 
+def test_prepack_batch_mixed_operands():
+    # one launch over operands of both load paths: 16-byte rows (K % 256 == 0; 28, 3 and
+    # 1 sixteen-column pieces per row) and byte rows (K / 16 = 3, 20, 25); each output
+    # byte-for-byte the oracle's, the 64 guard bytes after each untouched
+    shapes = [(300, 7168), (129, 768), (7, 48), (1000, 320), (128, 256), (257, 400), (40, 2048)]
+    rng = np.random.default_rng(77)
+    srcs, dsts, refs, guard = [], [], [], 64
+    for rows, K in shapes:
+        sf = rng.integers(0, 256, (rows, K // 16), dtype=np.uint8)
+        srcs.append(torch.from_numpy(sf).cuda())
+        refs.append(oracle.blocked_scales(sf))
+        dsts.append(torch.full((nv.nvfp4_prepacked_scale_bytes(rows, K) + guard,), 0xEE, dtype=torch.uint8,
+                               device="cuda"))
+    nv.nvfp4_prepack_scales_batch([s.data_ptr() for s in srcs], [r for r, _ in shapes], [k for _, k in shapes],
+                                  [d.data_ptr() for d in dsts])
+    torch.cuda.synchronize()
+    for (rows, K), d, ref in zip(shapes, dsts, refs):
+        got = d.cpu().numpy()
+        assert got.size - guard == ref.size
+        assert np.array_equal(got[:ref.size], ref), f"rows={rows} K={K}"
+        assert np.all(got[ref.size:] == 0xEE), f"rows={rows} K={K}: store past the blocked layout"
+
+
 # ------------------------------------------------------------ small, full ---
 
 def test_decode_sized_sets_take_the_swapped_kernel():
