@@ -157,7 +157,7 @@ __device__ __forceinline__ void stage_scales(const uint8_t *src, int sfa_bytes, 
             const int j = idx / kHalves, h = idx % kHalves;
 #pragma unroll
             for (int i = 0; i < 4; ++i)
-                rb[4 * x + i] = b[h].word<kRowMajor>(j, i);
+                rb[4 * x + i] = b[h].template word<kRowMajor>(j, i);
         }
         tmem_store_16cols(col + sfb_col + 16 * batch, rb);
     }
@@ -327,7 +327,7 @@ struct EpilogueStager {
 };
 
 template <int BN, int STAGES>
-__global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const __grid_constant__ KernelArgs args)
+__global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const __grid_constant__ SingleArgs args)
 {
     static_assert(BN == 128 || BN == 256, "BN must be 128 or 256");
     using L = Layout<BN, STAGES>;
@@ -354,7 +354,8 @@ __global__ void __launch_bounds__(kThreads, 1) nvfp4_grouped_gemm_kernel(const _
     // overlaps the set-up below.
     WorkItem first_item{};
     if (warp == kProducerWarp && lane == 0 && item_begin < item_end)
-        first_item = global_item(args, item_begin);
+        first_item = blockIdx.x < (unsigned)kSingleFirstItems ? item_of(args.first[blockIdx.x])
+                                                              : global_item(args, item_begin);
     // The operand maps of groups past those in the launch parameters, fetched ahead by
     // the producer warp's lanes in parallel.
     if (warp == kProducerWarp)

@@ -1157,6 +1157,24 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
     return note_use(g_tables.front(), stream);
 }
 
+// Each list's first item, copied from the host copy of the work items into the launch
+// parameters (lists past the array's length read theirs from the table).
+template <int N>
+void fill_first_items(FirstItem (&first)[N], const WorkItem *items, const uint32_t *list_begin, int lists)
+{
+    for (int l = 0; l < std::min(lists, N); ++l)
+        if (list_begin[l] < list_begin[l + 1])
+            first[l] = first_item_of(items[list_begin[l]]);
+}
+
+template <int N>
+void fill_first_items(FirstItem (&first)[N], const CachedTable &t)
+{
+    const TableHeader *th = static_cast<const TableHeader *>(t.host);
+    const WorkItem *items = reinterpret_cast<const WorkItem *>(static_cast<const uint8_t *>(t.host) + th->off_items);
+    fill_first_items(first, items, t.list_begin.data(), (int)t.list_begin.size() - 1);
+}
+
 // The A, B and C maps of the first kParamMapGroups groups, copied from the table's
 // host copy into the launch parameters.
 void fill_param_maps(KernelArgs &args, const void *host_table, int num_groups)
@@ -1194,7 +1212,7 @@ template <int BN, int STAGES>
 int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
 {
     using L = Layout<BN, STAGES>;
-    KernelArgs args{};
+    SingleArgs args{};
     args.table = static_cast<const Table *>(t.dev);
     args.items = table_items(t);
     args.status = ds.status;
@@ -1207,6 +1225,7 @@ int launch_gemm(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.counters = t.counters;
     fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
+    fill_first_items(args.first, t);
     CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<BN, STAGES>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     static_assert(kDeepStages128 == 5 && kDeepStages256 == 3, "kernel names below");
     g_last_kernel.store(BN == 128 ? (STAGES == 2 ? "nvfp4_grouped_gemm_kernel<128,2>" : "nvfp4_grouped_gemm_kernel<128,5>")
@@ -1238,16 +1257,6 @@ int prepare_pair_kernel(DeviceState &ds)
     return NVFP4_OK;
 }
 
-// Each list's first item, copied from the table's host copy into the launch parameters.
-void fill_first_items(PairArgs &args, const CachedTable &t)
-{
-    const TableHeader *th = static_cast<const TableHeader *>(t.host);
-    const WorkItem *items = reinterpret_cast<const WorkItem *>(static_cast<const uint8_t *>(t.host) + th->off_items);
-    const int lists = (int)t.list_begin.size() - 1;
-    for (int l = 0; l < std::min(lists, kParamFirstItems); ++l)
-        if (t.list_begin[l] < t.list_begin[l + 1])
-            args.first[l] = first_item_of(items[t.list_begin[l]]);
-}
 
 int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
 {
@@ -1264,7 +1273,7 @@ int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int 
     args.counters = t.counters;
     fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
-    fill_first_items(args, t);
+    fill_first_items(args.first, t);
     CUDA_TRY(launch_kernel(nvfp4_pair_gemm_kernel<kPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_pair_gemm_kernel<5>");
     return NVFP4_OK;
@@ -1336,7 +1345,7 @@ int launch_swap_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream,
     args.counters = t.counters;
     fill_param_maps(args, t.host, num_groups);
     std::copy(t.list_begin.begin(), t.list_begin.end(), args.list_begin);
-    fill_first_items(args, t);
+    fill_first_items(args.first, t);
     CUDA_TRY(launch_kernel(nvfp4_swapab_pair_kernel<kSwapPairStages>, (unsigned)t.grid, L::kSmemBytes, stream, args));
     static_assert(kSwapPairStages == 5, "kernel name below");
     g_last_kernel.store("nvfp4_swapab_pair_kernel<5>");
@@ -1934,7 +1943,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     // buffer may be reused by the next call.
     CUDA_TRY(cudaMemcpyAsync(dscratch + kNoAllocStatusBytes, h, total, cudaMemcpyHostToDevice, stream));
 
-    KernelArgs args{};
+    SingleArgs args{};
     args.table = dtable;
     args.items = reinterpret_cast<const int4 *>(reinterpret_cast<const uint8_t *>(dtable) + off_items);
     args.status = dstatus;
@@ -1946,6 +1955,7 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     args.counters = nullptr;
     std::copy(cta_begin, cta_begin + lists + 1, args.list_begin);
     fill_param_maps(args, h, (int)ngroups);
+    fill_first_items(args.first, items, cta_begin, (int)lists);
     CUDA_TRY(launch_kernel(nvfp4_grouped_gemm_kernel<kDefaultBlockN, kDefaultStages>, (unsigned)grid,
                            Layout<kDefaultBlockN, kDefaultStages>::kSmemBytes, stream, args));
     g_last_kernel.store("nvfp4_grouped_gemm_kernel<128,5>");

@@ -137,8 +137,8 @@ struct KernelArgs {
 };
 
 // The fields of a list's first work item that the TMA producer needs for its first
-// copies, in the CTA-pair kernels' launch parameters: the producer's first copy then
-// waits for no load from the (cold) table. 48 bytes a list.
+// copies, in the launch parameters of the CTA-pair kernels and of the single-CTA kernel:
+// the producer's first copy then waits for no load from the (cold) table. 48 bytes a list.
 struct FirstItem {
     int32_t group, tile_m, tile_n, kb_begin, kb_end, kblocks64, flags, a_row;
     const uint8_t *sfa;
@@ -148,6 +148,12 @@ constexpr int kParamFirstItems = 80;  // lists (CTA pairs) whose first item trav
 
 struct PairArgs : KernelArgs {
     FirstItem first[kParamFirstItems];
+};
+
+constexpr int kSingleFirstItems = 160;  // lists (CTAs) of the single-CTA kernel, the same way
+
+struct SingleArgs : KernelArgs {
+    FirstItem first[kSingleFirstItems];
 };
 
 __host__ __device__ inline FirstItem first_item_of(const WorkItem &w)
