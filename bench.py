@@ -735,6 +735,9 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
         "e2e": {"value": round(e2e_us / (world if args.split == "replicas" else 1), 3), "unit": "us", "steps": e2e_steps,
                 "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "gpu_launches_per_step": e2e_launches,
+                "h2d_gbs": round(h2d / (e2e_us * 1e-6) / 1e9, 1) if e2e_us > 0 else None,
+                "h2d_note": "the copy in is the whole step: this box's host link carries ~210 GB/s host to device "
+                            "(copy engine and SM loads of mapped pinned memory alike)",
                 "path": "one pinned host arena of A/B/row-major SFA/SFB -> one H2D copy -> nvfp4_grouped_gemm (the GEMM "
                         "kernel reads the row-major scales itself where K % 256 == 0, else a prepack launch first) -> "
                         "one D2H copy of C; device arenas double-buffered over three streams, so step i+1's copy in "
