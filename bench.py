@@ -545,6 +545,7 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
         nv.nvfp4_grouped_gemm(probs, stream)
     torch.cuda.synchronize()
     kernel = nv.nvfp4_last_kernel()
+    launches_per_call = nv.nvfp4_last_launches()  # this library's kernels per grouped call (the same every call)
     st, detail = nv.nvfp4_device_status(stream)
     if st != 0:
         raise RuntimeError(f"device status {st} {detail}")
@@ -720,7 +721,7 @@ def _run_ours(args, groups, rank, world, local_rank, clocks):
                      "frac": round(achieved_gbs / peaks["hbm_gbs"], 4), "peak_kind": f"{peak_kind} (copy bandwidth)",
                      "algorithmic_bytes_per_launch": nbytes, "traffic": profiled_traffic(kernel, args.workload),
                      "kernel": kernel},
-        "gpu_launches": args.steps,
+        "gpu_launches": launches_per_call * args.steps,
         "time_share": {"gemm": round(sum(per_call_ms) / (sum(per_call_ms) + sum(flush_ms)), 4),
                        "l2_flush": round(sum(flush_ms) / (sum(per_call_ms) + sum(flush_ms)), 4)},
         "timed_region_wall_s": round(wall, 3),
