@@ -52,7 +52,7 @@ struct Options {
     std::atomic<int64_t> timeout_us{2000000};
     std::atomic<int64_t> fault_skip_load{-1};
     std::atomic<int64_t> prefetch_stages{-1};  // -1 = automatic
-    std::atomic<int64_t> split_tail{1};  // 0 off, 1 single CTAs only, 2 single CTAs and pairs
+    std::atomic<int64_t> split_tail{1};  // 0 off, 1 single CTAs only, 2 single CTAs and pairs, 3 fill (single CTAs)
     std::atomic<int64_t> cta_pair{0};  // 0 = automatic, 1 = CTA pairs, 2 = single CTAs
     std::atomic<int64_t> sf_direct{1};  // 1 = row-major scales read by the GEMM kernel where K % 256 == 0
     std::atomic<int64_t> pdl{0};  // 1 = GEMM launches with programmatic stream serialization
@@ -560,8 +560,12 @@ struct Schedule {
 // same number of tail stages: CTA c takes stages [c*W/G, (c+1)*W/G) of the
 // tail's W stages. A tail tile that lands on several CTAs is a split tile: its
 // segments write fp32 partials and the last to finish stores C. Otherwise (mixed
-// K, T <= G, or split_tail off) every tile goes whole to CTA t % G.
-Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int block_n, int grid_cap, bool split_tail)
+// K, T <= G, or split off) every tile goes whole to CTA t % G.
+// split: kSplitNone, kSplitTail (the above), or kSplitFill: the same, and with fewer
+// tiles than CTAs the grid stays at grid_cap and every tile joins the tail, so that
+// the whole grid shares the K-stages (the small-grid fill).
+constexpr int kSplitNone = 0, kSplitTail = 1, kSplitFill = 2;
+Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int block_n, int grid_cap, int split)
 {
     struct Tile {
         int group, m, n, nk;
@@ -581,8 +585,8 @@ Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int blo
         uniform = uniform && t.nk == tiles[0].nk;
     // Split only where it shortens the busiest CTA by at least an eighth (and two
     // stages): each split costs a partial write and a reduction. With fewer tiles than
-    // CTAs nothing is split: spreading every tile over the whole grid this way measured
-    // slower (two-group K = 4096 set: 21.1 us against 15.3 whole).
+    // CTAs only the fill mode splits: spreading every tile over the whole grid measured
+    // slower on the two-group sets (K = 4096: 21.1 us against 15.3 whole), so it is opt-in.
     auto split_pays = [&](int G) {
         const int64_t nk = tiles[0].nk;
         const int64_t unbalanced = (int64_t)((T + G - 1) / G) * nk;
@@ -590,9 +594,11 @@ Schedule build_schedule(const std::vector<ActiveGroup> &gs, int block_m, int blo
         return unbalanced - balanced >= 2 && (unbalanced - balanced) * 8 >= unbalanced;
     };
     sc.grid = std::max(1, std::min<int>((int)T, grid_cap));
+    if (split == kSplitFill && uniform && T > 0 && T < (size_t)grid_cap && split_pays(grid_cap))
+        sc.grid = grid_cap;
     const int G = sc.grid, lists = G * kPipes;
     size_t whole = T;
-    if (split_tail && uniform && T > (size_t)G && T % G != 0 && split_pays(G))
+    if (split != kSplitNone && uniform && T % G != 0 && (T > (size_t)G || split == kSplitFill) && split_pays(G))
         whole = (T / G) * G;
     // Split segments go at the head of their CTA's list: their partial writes and
     // reductions then overlap the whole tiles that follow instead of ending the launch.
@@ -893,10 +899,14 @@ Plan plan_for(int variant, const DeviceState &ds, int64_t max_ctas)
 // kernel the fp32 partials of 256 x 256 tiles (their write, the reduction's
 // reads) cost more than the balance gains: on the MoE-shaped set with K = 7168
 // it measured 40.5 us split against 38.0 us whole. So pairs split only when
-// asked to (split_mode 2).
-bool split_for(int variant, int split_mode)
+// asked to (split_mode 2). split_mode 3 asks for the small-grid fill on single CTAs.
+int split_for(int variant, int split_mode)
 {
-    return split_mode == 2 || (split_mode == 1 && variant != kVariantPair);
+    if (split_mode == 2)
+        return kSplitTail;
+    if (variant == kVariantPair)
+        return kSplitNone;
+    return split_mode == 1 ? kSplitTail : split_mode == 3 ? kSplitFill : kSplitNone;
 }
 
 // Estimated time of a schedule's busiest list, in microseconds: stage_us per
@@ -1640,7 +1650,7 @@ extern "C" int nvfp4_set_option(int option, int64_t value)
         g_opt.timeout_us = value;
         return NVFP4_OK;
     case NVFP4_OPT_SPLIT_TAIL:
-        if (value < 0 || value > 2)
+        if (value < 0 || value > 3)
             return NVFP4_ERR_INVALID_ARG;
         g_opt.split_tail = value;
         return NVFP4_OK;

@@ -220,7 +220,12 @@ int nvfp4_last_a_maps(void);
  *                             does the same work (fp32 partials in a library-owned
  *                             workspace, summed in K order: results are deterministic).
  *                             It is applied only where it saves at least an eighth of
- *                             the busiest CTA's work.
+ *                             the busiest CTA's work. 3 = the small-grid fill on single
+ *                             CTAs (pairs: off): the same, and where there are fewer
+ *                             tiles than SMs the grid stays at one CTA per SM and every
+ *                             tile is cut, so that all SMs share the K-stages; it
+ *                             measured slower on the two-group shapes than whole tiles
+ *                             on fewer SMs, hence opt-in.
  *  NVFP4_OPT_WAIT_TIMEOUT_US: the bound of every wait inside the kernel
  *                             (default 2,000,000 us)
  *  NVFP4_OPT_SF_DIRECT     : 1 = row-major scales are read directly by the GEMM

@@ -5,6 +5,8 @@
 //    slots; a whole tile has split = -1;
 //  * with split_tail on and uniform K, the CTAs' stage counts differ by at most one
 //    plus one tile's worth less than the whole-tile share, i.e. max - min <= nk;
+//  * the small-grid fill keeps the whole grid when there are fewer tiles than CTAs and
+//    leaves every CTA within one stage of the even share;
 //  * the list offsets are monotone and end at the item count;
 //  * M-fusion runs form where A rows follow one another, and only there.
 #include "nvfp4_gemm.cu"
@@ -25,7 +27,7 @@ static int fails = 0;
         }                                        \
     } while (0)
 
-static void check(const std::vector<ActiveGroup> &gs, int bm, int bn, int cap, bool split)
+static void check(const std::vector<ActiveGroup> &gs, int bm, int bn, int cap, int split)
 {
     Schedule sc = build_schedule(gs, bm, bn, cap, split);
     const int lists = sc.grid * kPipes;
@@ -290,6 +292,26 @@ int main()
     for (auto cap : {70, 72, 36, 37, 7, 152})
         for (auto &sh : shapes)
             check(t4, sh[0], sh[1], cap, true);
+    // the small-grid fill (split mode 3 on single CTAs): the two-group K = 4096 set's 120
+    // tiles of 128 x 128 spread over all 152 CTAs, every CTA within one stage of the even
+    // share; with the tail mode alone the grid stays at 120 CTAs of whole tiles
+    {
+        const std::vector<ActiveGroup> g2 = {G(192, 3072, 4096), G(320, 3072, 4096)};
+        const Schedule f = build_schedule(g2, 128, 128, 152, kSplitFill);
+        CHECK(f.grid == 152 && f.splits > 0, "fill: grid %d, %d split tiles", f.grid, f.splits);
+        const Schedule t = build_schedule(g2, 128, 128, 152, kSplitTail);
+        CHECK(t.grid == 120 && t.splits == 0, "tail: grid %d, %d split tiles", t.grid, t.splits);
+        check(g2, 128, 128, 152, kSplitFill);
+        // one tile: spread where it pays (16 stages over 152 CTAs saves 15), at least the tile itself
+        const std::vector<ActiveGroup> one = {G(100, 128, 4096)};
+        CHECK(build_schedule(one, 128, 128, 152, kSplitFill).grid > 1, "fill of a single tile");
+        for (auto cap : {152, 100, 37, 1})
+            for (auto &sh : shapes)
+                check(t4, sh[0], sh[1], cap, kSplitFill);
+        CHECK(split_for(0, 3) == kSplitFill && split_for(kVariantPair, 3) == kSplitNone && split_for(0, 1) == kSplitTail &&
+                  split_for(kVariantPair, 2) == kSplitTail && split_for(0, 0) == kSplitNone,
+              "split_for");
+    }
     // the pair kernel's split test set (256 x 256 tiles): 8 + 4 + 6 + 3 = 21 tiles at K = 2048,
     // so 19 and 20 pairs split the short last wave, 21 and more do not
     CHECK(build_schedule(t4, 256, 256, 19, true).splits > 0 && build_schedule(t4, 256, 256, 20, true).splits > 0, "pair split");

@@ -100,7 +100,7 @@ def test_options(nv):
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_BLOCK_N, 64) == -1
     assert lib.nvfp4_set_option(99, 1) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 5) == -1
-    assert lib.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 3) == -1
+    assert lib.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 4) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, -1) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_WAIT_TIMEOUT_US, 0) == -1
     assert lib.nvfp4_set_option(nv.NVFP4_OPT_SF_DIRECT, 2) == -1
@@ -114,7 +114,8 @@ def test_options(nv):
                      (nv.NVFP4_OPT_FAULT_SKIP_LOAD, -1), (nv.NVFP4_OPT_BLOCK_N, 0),
                      (nv.NVFP4_OPT_CTA_PAIR, 1), (nv.NVFP4_OPT_CTA_PAIR, 2), (nv.NVFP4_OPT_CTA_PAIR, 3),
                      (nv.NVFP4_OPT_CTA_PAIR, 4), (nv.NVFP4_OPT_CTA_PAIR, 0),
-                     (nv.NVFP4_OPT_SPLIT_TAIL, 2), (nv.NVFP4_OPT_SPLIT_TAIL, 0), (nv.NVFP4_OPT_SPLIT_TAIL, 1),
+                     (nv.NVFP4_OPT_SPLIT_TAIL, 2), (nv.NVFP4_OPT_SPLIT_TAIL, 3), (nv.NVFP4_OPT_SPLIT_TAIL, 0),
+                     (nv.NVFP4_OPT_SPLIT_TAIL, 1),
                      (nv.NVFP4_OPT_SF_DIRECT, 0), (nv.NVFP4_OPT_SF_DIRECT, 1), (nv.NVFP4_OPT_PDL, 1),
                      (nv.NVFP4_OPT_PDL, 0), (nv.NVFP4_OPT_M_FUSION, 0), (nv.NVFP4_OPT_M_FUSION, 1)]:
         assert lib.nvfp4_set_option(opt, val) == 0

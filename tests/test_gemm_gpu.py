@@ -378,6 +378,31 @@ def test_full_size_workloads_every_output(name, pair, layout):
 
 # --------------------------------------------------------- split tail tiles ---
 
+@pytest.mark.parametrize("name", ["g2_n3072_k4096", "ragged"])
+def test_small_grid_fill_matches_oracle_and_is_deterministic(name):
+    # NVFP4_OPT_SPLIT_TAIL = 3 on single CTAs: fewer tiles than SMs, so the grid stays at
+    # one CTA per SM and every tile is cut along K. The two-group K = 4096 set's 120 tiles
+    # of 16 stages become 13 stages per CTA; the ragged set's 20 tiles of 8 stages become
+    # one- or two-stage segments on every SM. Every output against the oracle, and the
+    # same bits on a rerun (partials summed in K order).
+    if name == "ragged":
+        groups = gen.make_problem_set(44, [130, 60], [1024, 520], [2048, 2048])
+    else:
+        groups = gen.make_workload(name)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, 2)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 3)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    assert nv.nvfp4_last_kernel() == "nvfp4_grouped_gemm_kernel<128,5>"
+    check_full(groups, d, f"fill {name}")
+    first = [x.result().copy() for x in d]
+    for x in d:
+        x.reset()
+    run(d)
+    for f, x in zip(first, d):
+        assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
+
+
 @pytest.mark.parametrize("block_n,max_ctas", [(128, 70), (128, 72), (256, 36), (256, 37), (128, 0), (256, 7),
                                                ("pair", 38), ("pair", 40), ("pair", 0)])
 def test_split_tail_tiles_match_oracle_and_are_deterministic(block_n, max_ctas):
