@@ -433,3 +433,43 @@ def test_split_tail_tiles_match_oracle_and_are_deterministic(block_n, max_ctas):
         check_full(groups, e, "split off")
     finally:
         nv.nvfp4_set_option(nv.NVFP4_OPT_SPLIT_TAIL, 1)
+
+
+# ------------------------------------------------------- host threads, streams ---
+
+def test_concurrent_calls_from_host_threads():
+    # Four host threads, each with its own stream and problem set (one taking CTA pairs, one
+    # single CTAs, one the swapped-operand kernel, one with row-major scales read in the
+    # kernel), call the library five times each at the same time (ctypes drops the GIL).
+    # The table cache, the buffer pool and the per-stream events are shared under the
+    # library's lock; every output must still match the oracle.
+    import threading
+    specs = [(501, [200, 130, 256], [1024, 512, 768], [2048] * 3, nv.NVFP4_SF_PREPACKED),
+             (502, [64, 128], [512, 384], [1024, 1024], nv.NVFP4_SF_PREPACKED),
+             (503, [8, 16, 4], [1024, 512, 256], [2048, 1024, 512], nv.NVFP4_SF_PREPACKED),
+             (504, [40, 129], [264, 136], [512, 1024], nv.NVFP4_SF_ROWMAJOR)]
+    sets = [gen.make_problem_set(seed, Ms, Ns, Ks) for seed, Ms, Ns, Ks, _ in specs]
+    devs = [[DeviceGroup(g, layout) for g in s] for s, (_, _, _, _, layout) in zip(sets, specs)]
+    streams = [torch.cuda.Stream() for _ in specs]
+    for s in streams:
+        s.wait_stream(torch.cuda.current_stream())  # the inputs and the NaN-filled C are ready
+    errors = []
+
+    def worker(i):
+        try:
+            probs = [x.problem() for x in devs[i]]
+            for _ in range(5):
+                nv.nvfp4_grouped_gemm(probs, streams[i].cuda_stream)
+        except Exception as e:  # reported below, on the test's thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(len(specs))]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join()
+    torch.cuda.synchronize()
+    assert not errors, errors
+    assert nv.nvfp4_device_status()[0] == 0
+    for i, (s, d) in enumerate(zip(sets, devs)):
+        check_full(s, d, f"thread {i}")
