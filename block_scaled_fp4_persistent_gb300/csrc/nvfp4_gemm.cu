@@ -381,6 +381,30 @@ int get_encoder()
     return NVFP4_OK;
 }
 
+// The tensor-map encoder is a driver call. Runtime calls bind the device's primary
+// context to a host thread lazily, driver calls do not: in a thread that has made no
+// context-binding runtime call yet (a worker thread whose first call to this library
+// misses the table cache) the encoder fails with CUDA_ERROR_INVALID_CONTEXT. So before
+// encoding, a thread with no current context gets the primary context of `dev` bound,
+// as the runtime would have done; a context that the caller made current stays.
+int ensure_context(int dev)
+{
+    using CtxGetCurrent = CUresult (*)(CUcontext *);
+    static const CtxGetCurrent get_current = []() -> CtxGetCurrent {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q{};
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &fn, 12000, cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess)
+            return nullptr;
+        return reinterpret_cast<CtxGetCurrent>(fn);
+    }();
+    CUcontext ctx = nullptr;
+    if (get_current && get_current(&ctx) == CUDA_SUCCESS && ctx)
+        return NVFP4_OK;
+    CUDA_TRY(cudaSetDevice(dev));
+    return NVFP4_OK;
+}
+
 // A row-major uint8 matrix [rows][row_bytes] read as boxes of 128 bytes x box_rows,
 // with the 128-byte swizzle the MMA's K-major operand layout expects.
 int encode_operand_map(CUtensorMap *map, const void *base, uint64_t row_bytes, uint64_t rows, uint32_t box_rows)
@@ -1022,6 +1046,8 @@ int get_table(int dev, const DeviceState &ds, const std::vector<ActiveGroup> &gs
         it = g_table_index.end();
     }
     if (int rc = get_encoder())
+        return rc;
+    if (int rc = ensure_context(dev))
         return rc;
 
     // The pair kernel (variant kVariantPair) runs 256 x 256 tiles, one list per CTA pair.
@@ -1879,6 +1905,8 @@ extern "C" int nvfp4_grouped_gemm_noalloc(int g, const Nvfp4Problem *probs, nvfp
     if (ngroups == 0)
         return NVFP4_OK;
     if (int rc = get_encoder())
+        return rc;
+    if (int rc = ensure_context(dev))
         return rc;
 
     // Build the table in the static host buffer, with the same tile order and

@@ -300,6 +300,25 @@ def test_repeated_calls_and_table_cache():
     check_full(gb, db, "second problem set")
 
 
+
+def test_table_cache_churn_evicts_and_reuses_buffers():
+    # 40 problem sets (distinct C buffers, so distinct tables), called round-robin three
+    # times: past the cache's 32 tables every miss evicts one, whose pooled buffers go back
+    # to the pool once the stream event recorded after their last launch completes, and are
+    # handed to later tables. Every output of the last round against the oracle.
+    sets = [gen.make_problem_set(600 + i, [64 + i], [128 + 8 * (i % 4)], [256]) for i in range(40)]
+    devs = [[DeviceGroup(g) for g in s] for s in sets]
+    for _ in range(3):
+        for d in devs:
+            for x in d:
+                x.reset()
+            nv.nvfp4_grouped_gemm([x.problem() for x in d])
+    torch.cuda.synchronize()
+    assert nv.nvfp4_device_status()[0] == 0
+    for i, (s, d) in enumerate(zip(sets, devs)):
+        check_full(s, d, f"set {i}")
+
+
 def test_many_groups():
     rng = np.random.default_rng(3)
     Ms = [int(m) for m in rng.integers(1, 300, 40)]
