@@ -272,7 +272,9 @@ enum {
 int nvfp4_set_option(int option, int64_t value);
 
 /* Frees every cached table and workspace of every device. Synchronises each
- * device that holds one. Calls made afterwards start again from empty caches. */
+ * device that holds one. Calls made afterwards start again from empty caches.
+ * A CUDA graph that captured calls of this library reads their tables when it is
+ * replayed: do not replay such a graph after nvfp4_release (capture it again). */
 void nvfp4_release(void);
 
 /* The grouped GEMM for callers that cannot allocate device memory. The pages

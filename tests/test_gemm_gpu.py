@@ -319,6 +319,26 @@ def test_table_cache_churn_evicts_and_reuses_buffers():
         check_full(s, d, f"set {i}")
 
 
+
+def test_release_then_reuse():
+    # nvfp4_release frees every table, pooled buffer, workspace and the error word; the
+    # next calls rebuild them (a kernel kind that splits, so a workspace exists too)
+    ga = gen.make_problem_set(611, [130, 60, 200, 129], [2048, 1024, 1536, 520], [2048] * 4)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_MAX_CTAS, 70)  # a short last wave: split tiles, a workspace
+    da = [DeviceGroup(g) for g in ga]
+    run(da)
+    first = [x.result().copy() for x in da]
+    nv.nvfp4_release()
+    nv.nvfp4_release()  # twice: nothing left to free
+    for x in da:
+        x.reset()
+    run(da)
+    for f, x in zip(first, da):
+        assert np.array_equal(f.view(np.uint16), x.result().view(np.uint16))
+    check_full(ga, da, "after release")
+    assert nv.nvfp4_device_status()[0] == 0
+
+
 def test_many_groups():
     rng = np.random.default_rng(3)
     Ms = [int(m) for m in rng.integers(1, 300, 40)]
