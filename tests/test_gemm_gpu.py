@@ -339,6 +339,23 @@ def test_release_then_reuse():
     assert nv.nvfp4_device_status()[0] == 0
 
 
+
+@pytest.mark.parametrize("pair", [0, 1, 2, 3])
+def test_150_groups_every_kernel_kind(pair):
+    # groups 0-7 take their tensor maps from the launch parameters, the rest from the table
+    # with an acquire fence (and only those below 64 are prefetched): 150 small groups,
+    # ragged M and N, three K values, on every kernel kind
+    rng = np.random.default_rng(150)
+    Ms = [int(m) for m in rng.integers(1, 200, 150)]
+    Ns = [int(n) * 8 for n in rng.integers(1, 40, 150)]
+    Ks = [[256, 512, 1024][int(k)] for k in rng.integers(0, 3, 150)]
+    groups = gen.make_problem_set(151, Ms, Ns, Ks)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    check_full(groups, d, f"150 groups, kind {pair}")
+
+
 def test_many_groups():
     rng = np.random.default_rng(3)
     Ms = [int(m) for m in rng.integers(1, 300, 40)]
