@@ -244,6 +244,38 @@ def test_structured_closed_form():
         assert np.all(dg.result().astype(np.float64) == g.K)
 
 
+
+@pytest.mark.parametrize("pair", [1, 2])
+def test_large_closed_form_with_row_and_column_scales(pair):
+    # Every element 1.0; A's scale depends on the row (0.5, 1, 2 for m % 3) and B's on the
+    # column (0.25, 0.5, 1, 2 for n % 4), so C[m][n] = K * sa[m] * sb[n] exactly (a power of
+    # two times K, at most 2^15). A 2048 x 8192 x 8192 group (hundreds of tiles, several
+    # waves, the compute-heavy regime) and a ragged one; every output compared, which also
+    # catches a row or column of outputs landing in the wrong place.
+    class G:
+        pass
+    groups = []
+    for M, N, K in [(2048, 8192, 8192), (300, 1000, 4096)]:
+        g = G()
+        g.M, g.N, g.K = M, N, K
+        g.A = np.full((M, K // 2), 0x22, np.uint8)
+        g.B = np.full((N, K // 2), 0x22, np.uint8)
+        g.SFA = np.repeat(np.array([0x30, 0x38, 0x40], np.uint8)[np.arange(M) % 3][:, None], K // 16, axis=1)
+        g.SFB = np.repeat(np.array([0x28, 0x30, 0x38, 0x40], np.uint8)[np.arange(N) % 4][:, None], K // 16, axis=1)
+        groups.append(g)
+    nv.nvfp4_set_option(nv.NVFP4_OPT_CTA_PAIR, pair)
+    d = [DeviceGroup(g) for g in groups]
+    run(d)
+    for g, dg in zip(groups, d):
+        sa = np.array([0.5, 1.0, 2.0])[np.arange(g.M) % 3]
+        sb = np.array([0.25, 0.5, 1.0, 2.0])[np.arange(g.N) % 4]
+        expect = g.K * sa[:, None] * sb[None, :]
+        got = dg.result().astype(np.float64)
+        bad = np.argwhere(got != expect)
+        assert bad.size == 0, f"kind {pair} M={g.M}: {len(bad)} outputs wrong, first at {tuple(bad[0])}"
+        assert dg.guards_intact()
+
+
 @pytest.mark.parametrize("block_n", [128, 256])
 @pytest.mark.parametrize("stages", [2, 0])
 @pytest.mark.parametrize("max_ctas", [1, 3, 0])
