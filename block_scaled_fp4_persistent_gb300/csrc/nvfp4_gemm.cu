@@ -1293,7 +1293,6 @@ int prepare_pair_kernel(DeviceState &ds)
     return NVFP4_OK;
 }
 
-
 int launch_pair(DeviceState &ds, const CachedTable &t, cudaStream_t stream, int num_groups)
 {
     using L = PairLayout<kPairStages>;
