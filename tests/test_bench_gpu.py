@@ -74,3 +74,18 @@ def test_prepack_and_cold_call_legs(line):
     assert p["algorithmic_bytes"] == p["read_bytes"] + p["written_bytes"]
     cc = line["cold_call"]
     assert positive(cc["miss"]["gpu_us"]) and positive(cc["hit"]["gpu_us"])
+
+
+@pytest.mark.parametrize("split", ["groups", "n"])
+def test_split_modes_run_at_one_rank(split):
+    # --split shards one call across the ranks; with one rank the share is the whole call,
+    # and the line says so (strong scaling, the sharding in `parallelism`)
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--steps", "10", "--warmup", "3", "--split", split,
+                        "--no-cpu-baseline", "--no-other-workloads", "--e2e-steps", "2"],
+                       capture_output=True, text=True, timeout=900, cwd=ROOT)
+    assert r.returncode == 0, r.stderr[-2000:]
+    lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
+    assert len(lines) == 1
+    d = json.loads(lines[0])
+    assert d["scaling"] == "strong" and split in d["config"]["parallelism"]
+    assert positive(d["value"]) and d["config"]["workload"] == "moe_g8_n4096_k7168"
